@@ -1,0 +1,407 @@
+#!/usr/bin/env python3
+"""Benchmark of the C128 compressor (compress -> RMSNorm -> FP8/UE8M0 + RoPE -> paged store).
+
+Workload: the all-boundary sweep at token_num = 16374 — each token its own request at a window
+end, 16 distinct state blocks per token (8.58 GB of fp32 state read per call), kv block size 2.
+A step is one call of the whole path (plan kernel + compress kernel) on inputs already resident
+in HBM. The state is larger than L2, so no flush is needed between steps.
+
+Prints one JSON line: compressed windows/s (whole job), ms per step, the dominant kernel's
+roofline (algorithmic bytes / CUDA-event kernel time vs the measured HBM copy bandwidth),
+an end-to-end figure through the public API with the per-step metadata uploaded from pinned host
+memory and the k_cache read back, SM clocks sampled during the timed region, the CPU oracle
+timed on a bounded sample of the same workload, and µs/call over the token_num sweep.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--no-sweep]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from deepseek_v4_sparse_c128_gb300 import inputs  # noqa: E402
+
+METRIC = "compressed windows/s and achieved HBM GB/s vs GB300 peak; µs per call vs token_num"
+UNIT = "windows/s"
+HEADLINE_T = 16374
+STATE_BYTES_PER_WINDOW = 128 * 1024 * 4                       # 524,288
+ALGO_BYTES_PER_WINDOW = STATE_BYTES_PER_WINDOW + 64 + 256 + 584  # + block ids, cos/sin row, k_cache write
+PAGES_US_16374 = 1425.900  # vLLM PR #44230, Performance table (B300), token_num 16374
+KERNEL_SRC = os.path.join(ROOT, "deepseek_v4_sparse_c128_gb300", "csrc", "c128_kernels.cu")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "compress_kernel_traffic.json")
+
+
+def workload_config(T: int, n_gpus: int) -> dict:
+    return {"workload": f"sweep{T}: all-boundary, token_num {T}, each token its own request at a window end, "
+                        f"16 distinct fp32 state blocks per token ({T * STATE_BYTES_PER_WINDOW / 1e9:.2f} GB of "
+                        f"state per call), kv block size 2",
+            "token_num": T, "active_windows": T, "kv_block_size": 2, "state_block_size": 8, "head": 512,
+            "l2": "inputs larger than L2 (state read per call >> 129 MB)", "parallelism": f"replicas x{n_gpus}"}
+
+
+# ------------------------------------------------------------------------------- distributed
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        import torch
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return ws, rank, local
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def reduce_max_sum(ws, local_ms: float, local_units: float):
+    """(max over ranks of the timed-region length, sum over ranks of the units processed)."""
+    if ws == 1:
+        return local_ms, local_units
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([local_ms], dtype=torch.float64, device=dev)
+    u = torch.tensor([local_units], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
+
+
+# ------------------------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi samples every 200 ms while the timed region runs."""
+    FIELDS = ("uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid: str):
+        self.uuid = uuid
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader",
+                                          "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+            self.reader = threading.Thread(target=self._read, daemon=True)
+            self.reader.start()
+            time.sleep(0.3)
+        except FileNotFoundError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        return False
+
+    def summary(self) -> dict:
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9 or (self.uuid and self.uuid not in parts[0]):
+                continue
+            try:
+                sm.append(float(parts[1].split()[0]))
+                mx.append(float(parts[2].split()[0]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------------------- CPU oracle
+def oracle_sample_problem(p, sample, state_blocks):
+    """A compact problem holding only the sampled windows (their 16 blocks each)."""
+    S = sample.size
+    first = (p.positions[sample] - 127) // 8
+    bt = np.zeros((S, p.block_table.shape[1]), np.int32)
+    for i in range(S):
+        bt[i, first[i]:first[i] + 16] = np.arange(16 * i, 16 * i + 16)
+    return inputs.Problem("sample", np.arange(S, dtype=np.int32), p.positions[sample].copy(),
+                          p.slot_mapping[sample].copy(), bt, state_blocks, p.rms_w, p.eps, p.cos_sin,
+                          p.k_cache.copy(), p.kv_slot_mapping[sample].copy(), p.kv_block_size)
+
+
+def time_oracle(sub, threads: int, min_cpu_s: float = 10.0, max_wall_s: float = 60.0):
+    import oracle
+    oracle.build()
+    S = sub.num_tokens
+    windows, wall, passes = 0, 0.0, 0
+    cpu0 = time.process_time()
+    t0 = time.perf_counter()
+    while True:
+        kc = sub.k_cache.copy()
+        oracle.forward(sub, k_cache=kc, threads=threads)
+        windows += S
+        passes += 1
+        wall = time.perf_counter() - t0
+        if time.process_time() - cpu0 >= min_cpu_s or wall >= max_wall_s:
+            break
+    return windows / wall, passes, time.process_time() - cpu0
+
+
+def gather_blocks_to_host(p, state_dev, sample):
+    import torch
+    first = (p.positions[sample] - 127) // 8
+    blk = np.stack([p.block_table[int(t), first[i]:first[i] + 16] for i, t in enumerate(sample)]).reshape(-1)
+    idx = torch.from_numpy(blk.astype(np.int64)).to(state_dev.device)
+    return state_dev.index_select(0, idx).cpu().numpy()
+
+
+# --------------------------------------------------------------------------------- our arm
+def run_ours(args, ws, rank, local):
+    import torch
+    from deepseek_v4_sparse_c128_gb300 import binding, build
+
+    torch.cuda.set_device(local)
+    build.build()
+    binding.load()
+    dev = torch.device("cuda", local)
+    T = args.tokens
+    p = inputs.make_problem("sweep", seed=inputs.CONFIG_SEEDS["sweep"] + 7919 * rank, tokens=T, state_device=str(dev))
+    to = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    d = {k: to(getattr(p, k)) for k in ("token_to_req", "positions", "slot_mapping", "block_table", "rms_w",
+                                        "cos_sin", "k_cache", "kv_slot_mapping")}
+    d["state"] = p.state
+    stream = torch.cuda.current_stream()
+
+    def step():
+        binding.compress_norm_rope_store(d["token_to_req"], d["positions"], d["slot_mapping"], d["block_table"],
+                                         d["state"], d["rms_w"], p.eps, d["cos_sin"], d["k_cache"],
+                                         d["kv_slot_mapping"], p.kv_block_size)
+
+    binding.reserve_workspace(T)
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert binding.device_errors(clear=True) == 0, "device error during warm-up"
+    uuid = str(getattr(torch.cuda.get_device_properties(dev), "uuid", "") or "")
+    uuid = uuid if uuid.startswith("GPU-") or not uuid else "GPU-" + uuid
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(uuid) as clocks:
+        barrier(ws)
+        torch.cuda.synchronize()
+        with binding.KernelTimer() as ktimer:
+            e0.record(stream)
+            for _ in range(args.steps):
+                step()
+            e1.record(stream)
+            torch.cuda.synchronize()
+        barrier(ws)
+    local_ms = e0.elapsed_time(e1)
+    assert binding.device_errors(clear=True) == 0, "device error in the timed region"
+    max_ms, total_windows = reduce_max_sum(ws, local_ms, float(T * args.steps))
+    value = total_windows / (max_ms / 1e3)
+    ms_per_step = max_ms / args.steps
+    kernel_ms = ktimer.total_ms / max(1, ktimer.launches)
+
+    # ---- end to end through the public API: per-step metadata from pinned host memory in, k_cache out
+    host = {k: torch.from_numpy(np.ascontiguousarray(getattr(p, k))).pin_memory()
+            for k in ("token_to_req", "positions", "slot_mapping", "block_table", "kv_slot_mapping")}
+    kc_host = torch.empty(d["k_cache"].shape, dtype=torch.uint8).pin_memory()
+    h2d = sum(int(v.numel() * v.element_size()) for v in host.values())
+    d2h = int(kc_host.numel())
+
+    def e2e_step():
+        for k, v in host.items():
+            d[k].copy_(v, non_blocking=True)
+        step()
+        kc_host.copy_(d["k_cache"], non_blocking=True)
+
+    e2e_steps = max(3, min(args.steps, 200))
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(ws)
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_s = time.perf_counter() - t0
+    barrier(ws)
+    e2e_max_ms, e2e_windows = reduce_max_sum(ws, e2e_s * 1e3, float(T * e2e_steps))
+
+    out = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+           "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+           "vs_baseline": value / (HEADLINE_T / (PAGES_US_16374 * 1e-6)) if T == HEADLINE_T else None,
+           "dtype": "f32", "data": "synthetic (seeded: kv~N(0,1), score~N(0,2), rms_w=1+0.1N(0,1))",
+           "config": workload_config(T, ws),
+           "us_per_call": ms_per_step * 1e3,
+           "hbm_gbs_per_gpu": T * ALGO_BYTES_PER_WINDOW / (ms_per_step * 1e-3) / 1e9,
+           "gpu_launches": 2 * args.steps}
+    out["e2e"] = {"value": e2e_windows / (e2e_max_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                  "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+                  "note": "state cache resident (it is a cache); per-step token metadata and block table in, "
+                          "whole k_cache out"}
+    peaks = {}
+    try:
+        peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+    except (OSError, ValueError):
+        pass
+    peak, peak_src = (float(peaks["hbm_gbs"]), "measured") if "hbm_gbs" in peaks else (6800.0, "fallback")
+    achieved = T * ALGO_BYTES_PER_WINDOW / (kernel_ms * 1e-3) / 1e9
+    out["roofline"] = {"bound": "hbm", "kernel": "compress_kernel", "achieved": achieved, "peak": peak,
+                       "peak_source": peak_src, "unit": "GB/s", "frac": achieved / peak,
+                       "traffic": traffic_per_launch(T), "kernel_us": kernel_ms * 1e3,
+                       "algorithmic_bytes_per_launch": T * ALGO_BYTES_PER_WINDOW}
+    out["clocks"] = clocks.summary()
+
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        rng = np.random.default_rng(11)
+        sample = np.sort(rng.choice(T, size=min(T, 1024), replace=False))
+        sub = oracle_sample_problem(p, sample, gather_blocks_to_host(p, p.state, sample))
+        threads = os.cpu_count() or 1
+        wps, passes, cpu_s = time_oracle(sub, threads)
+        out["cpu_baseline"] = {"value": wps, "unit": UNIT, "cores": threads, "kind": "oracle",
+                               "sample": f"{sample.size} random windows of sweep{T} x {passes} passes "
+                                         f"({cpu_s:.1f} s CPU), oracle over host threads"}
+    if not args.no_sweep and ws == 1:
+        del d, p
+        torch.cuda.empty_cache()
+        out["sweep_us_per_call"] = sweep(args, dev)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+
+
+def traffic_per_launch(T: int):
+    """DRAM bytes per launch from the committed ncu capture, scaled by windows, or None when the
+    kernel source changed since the capture."""
+    try:
+        rec = json.load(open(TRAFFIC_FILE))
+    except (OSError, ValueError):
+        return None
+    src_hash = hashlib.sha256(open(KERNEL_SRC, "rb").read()).hexdigest()
+    if rec.get("kernel_source_sha256") != src_hash:
+        return None
+    return rec["dram_bytes_per_window"] * T
+
+
+def sweep(args, dev):
+    """µs per call vs token_num with an L2 flush (a 512 MB write) before every timed call."""
+    import torch
+    from deepseek_v4_sparse_c128_gb300 import binding
+    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    res = {}
+    for T in inputs.SWEEP_TOKENS:
+        p = inputs.make_problem("sweep", tokens=T, state_device=str(dev))
+        to = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+        d = {k: to(getattr(p, k)) for k in ("token_to_req", "positions", "slot_mapping", "block_table", "rms_w",
+                                            "cos_sin", "k_cache", "kv_slot_mapping")}
+
+        def step():
+            binding.compress_norm_rope_store(d["token_to_req"], d["positions"], d["slot_mapping"], d["block_table"],
+                                             p.state, d["rms_w"], p.eps, d["cos_sin"], d["k_cache"],
+                                             d["kv_slot_mapping"], p.kv_block_size)
+        binding.reserve_workspace(T)
+        for _ in range(5):
+            step()
+        times = []
+        n = 50 if T < 4096 else 20
+        for _ in range(n):
+            flush.fill_(1.0)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            step()
+            b.record()
+            torch.cuda.synchronize()
+            times.append(a.elapsed_time(b) * 1e3)
+        res[str(T)] = round(statistics.mean(times), 3)
+        del d, p
+    assert binding.device_errors(clear=True) == 0
+    return res
+
+
+# --------------------------------------------------------------------------- reference arm
+def run_reference(args, ws, rank):
+    """The CPU oracle as it stands, on the host cores, over a bounded sample of the same workload."""
+    if rank != 0:
+        return
+    T = args.tokens
+    # metadata of the full workload; the state is drawn only for the sampled windows' blocks
+    p = inputs.make_problem("sweep", tokens=T, state_device="none")
+    rng = np.random.default_rng(12)
+    S = min(T, 256)
+    sample = np.sort(rng.choice(T, size=S, replace=False))
+    st = inputs.draw_state(99, 16 * S, "cpu")
+    sub = oracle_sample_problem(p, sample, st)
+    import oracle
+    oracle.build()
+    threads = os.cpu_count() or 1
+    for _ in range(args.warmup):
+        oracle.forward(sub, k_cache=sub.k_cache.copy(), threads=threads)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.forward(sub, k_cache=sub.k_cache.copy(), threads=threads)
+    wall = time.perf_counter() - t0
+    value = S * args.steps / wall
+    out = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+           "warmup": args.warmup, "ms_per_step": wall * 1e3 / args.steps, "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+           "config": workload_config(T, ws),
+           "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                            "sample": f"each step: {S} random windows of sweep{T} (state of their 16 blocks "
+                                      f"each), oracle over {threads} host threads"},
+           "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--tokens", type=int, default=HEADLINE_T)
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    ws, rank, local = dist_setup()
+    try:
+        if args.impl == "reference":
+            run_reference(args, ws, rank)
+        else:
+            run_ours(args, ws, rank, local)
+    finally:
+        if ws > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

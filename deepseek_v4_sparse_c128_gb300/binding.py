@@ -1,0 +1,203 @@
+"""ctypes binding of libc128compress (include/c128compress.h).
+
+Argument marshalling only: torch tensors (or raw device pointers) become ``c128_tensor_t``
+descriptors and the current torch CUDA stream becomes the call's stream. Every step of the op
+runs in the library's CUDA kernels; there is no fallback path, and importing this module fails
+loudly if the library cannot be loaded.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+from . import build as _build
+
+C128_I32, C128_I64, C128_F32, C128_U8 = 1, 2, 3, 4
+STATUS = {
+    0: "C128_OK", 1: "C128_ERR_NULL_PTR", 2: "C128_ERR_DTYPE", 3: "C128_ERR_SHAPE", 4: "C128_ERR_STRIDE",
+    5: "C128_ERR_ALIGN", 6: "C128_ERR_UNSUPPORTED", 7: "C128_ERR_ARG", 8: "C128_ERR_CUDA", 9: "C128_ERR_NOMEM",
+}
+DEV_BITS = {1: "BAD_REQ", 2: "BAD_BT_COL", 4: "BAD_BLOCK", 8: "BAD_COS_ROW", 16: "BAD_KV_SLOT", 32: "TIMEOUT"}
+
+# Every entry point the header declares, with its ctypes signature.
+EXPORTS = (
+    "compress_norm_rope_store",
+    "c128_compress_norm_rope_store_debug",
+    "c128_status_string",
+    "c128_reserve_workspace",
+    "c128_device_errors",
+    "c128_kernel_timer_begin",
+    "c128_kernel_timer_end",
+    "c128_get_info",
+    "c128_release_all",
+)
+
+
+class Tensor(ctypes.Structure):
+    _fields_ = [("data", ctypes.c_void_p), ("dtype", ctypes.c_int32), ("ndim", ctypes.c_int32),
+                ("shape", ctypes.c_int64 * 4), ("stride", ctypes.c_int64 * 4)]
+
+
+class Info(ctypes.Structure):
+    _fields_ = [("sm_count", ctypes.c_int32), ("threads", ctypes.c_int32), ("smem_bytes", ctypes.c_int32),
+                ("stages", ctypes.c_int32), ("ctas_per_sm", ctypes.c_int32),
+                ("plan_tokens_per_cta", ctypes.c_int32), ("wait_timeout_ms", ctypes.c_int32),
+                ("version", ctypes.c_int32)]
+
+
+class C128Error(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {STATUS.get(status, status)} ({lib().c128_status_string(status).decode()})")
+
+
+_lib = None
+
+
+def lib_path() -> str:
+    return _build.LIB
+
+
+def load(path: Optional[str] = None) -> ctypes.CDLL:
+    """Load the library (built in-tree by ``deepseek_v4_sparse_c128_gb300.build``)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = path or lib_path()
+    if not os.path.exists(path):
+        raise RuntimeError(f"libc128compress.so not found at {path}; run deepseek_v4_sparse_c128_gb300.build.build()")
+    L = ctypes.CDLL(path)
+    T = ctypes.POINTER(Tensor)
+    i64, vp = ctypes.c_int64, ctypes.c_void_p
+    L.compress_norm_rope_store.argtypes = [T, T, T, T, T, T, ctypes.c_float, T, T, T, i64, vp]
+    L.c128_compress_norm_rope_store_debug.argtypes = [T, T, T, T, T, T, ctypes.c_float, T, T, T, i64, T, vp]
+    L.c128_status_string.argtypes = [ctypes.c_int]
+    L.c128_status_string.restype = ctypes.c_char_p
+    L.c128_reserve_workspace.argtypes = [i64, vp]
+    L.c128_device_errors.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32), ctypes.c_int]
+    L.c128_kernel_timer_begin.argtypes = [vp]
+    L.c128_kernel_timer_end.argtypes = [vp, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int64)]
+    L.c128_get_info.argtypes = [ctypes.POINTER(Info)]
+    L.c128_release_all.argtypes = []
+    for name in EXPORTS:
+        if name != "c128_status_string":
+            getattr(L, name).restype = ctypes.c_int
+    _lib = L
+    return L
+
+
+def lib() -> ctypes.CDLL:
+    return load()
+
+
+# ----------------------------------------------------------------------------- marshalling
+_TORCH_DTYPES = None
+
+
+def _dtype_code(t) -> int:
+    global _TORCH_DTYPES
+    import torch
+    if _TORCH_DTYPES is None:
+        _TORCH_DTYPES = {torch.int32: C128_I32, torch.int64: C128_I64, torch.float32: C128_F32,
+                         torch.uint8: C128_U8}
+    if t.dtype not in _TORCH_DTYPES:
+        raise TypeError(f"unsupported dtype {t.dtype}")
+    return _TORCH_DTYPES[t.dtype]
+
+
+def describe(t) -> Tensor:
+    """c128_tensor_t of a torch tensor (any device; the library expects device memory)."""
+    d = Tensor()
+    d.data = t.data_ptr() if t.numel() > 0 else None
+    d.dtype = _dtype_code(t)
+    d.ndim = t.dim()
+    if d.ndim > 4:
+        raise ValueError("at most 4 dimensions")
+    for i in range(d.ndim):
+        d.shape[i] = t.shape[i]
+        d.stride[i] = t.stride(i)
+    return d
+
+
+def _stream_handle(stream) -> Optional[int]:
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _check(rc: int, where: str):
+    if rc != 0:
+        raise C128Error(rc, where)
+
+
+def compress_norm_rope_store(token_to_req_indices, positions, slot_mapping, block_table, state_cache, rms_w,
+                             eps: float, cos_sin_cache, k_cache, kv_slot_mapping, kv_block_size: int,
+                             stream=None, comp_out=None) -> None:
+    """Run the C128 compressor on CUDA tensors (see include/c128compress.h for the contract).
+    ``k_cache`` is updated in place. ``comp_out`` ([T, 512] fp32), if given, receives the fp32
+    compressed vectors of the stored tokens (the debug entry point)."""
+    L = lib()
+    args = [describe(x) for x in (token_to_req_indices, positions, slot_mapping, block_table, state_cache, rms_w)]
+    cs, kc, kvs = describe(cos_sin_cache), describe(k_cache), describe(kv_slot_mapping)
+    h = _stream_handle(stream)
+    refs = [ctypes.byref(a) for a in args]
+    if comp_out is None:
+        rc = L.compress_norm_rope_store(*refs, ctypes.c_float(eps), ctypes.byref(cs), ctypes.byref(kc),
+                                        ctypes.byref(kvs), int(kv_block_size), h)
+        _check(rc, "compress_norm_rope_store")
+    else:
+        co = describe(comp_out)
+        rc = L.c128_compress_norm_rope_store_debug(*refs, ctypes.c_float(eps), ctypes.byref(cs), ctypes.byref(kc),
+                                                   ctypes.byref(kvs), int(kv_block_size), ctypes.byref(co), h)
+        _check(rc, "c128_compress_norm_rope_store_debug")
+
+
+def call_status(*args, **kw) -> int:
+    """Like compress_norm_rope_store but returns the status code instead of raising."""
+    try:
+        compress_norm_rope_store(*args, **kw)
+        return 0
+    except C128Error as e:
+        return e.status
+
+
+def reserve_workspace(max_tokens: int, stream=None) -> None:
+    _check(lib().c128_reserve_workspace(int(max_tokens), _stream_handle(stream)), "c128_reserve_workspace")
+
+
+def device_errors(stream=None, clear: bool = True) -> int:
+    bits = ctypes.c_uint32(0)
+    _check(lib().c128_device_errors(_stream_handle(stream), ctypes.byref(bits), int(clear)), "c128_device_errors")
+    return int(bits.value)
+
+
+class KernelTimer:
+    """Sum of compress-kernel times (CUDA events on the launching stream) between enter and exit."""
+
+    def __init__(self, stream=None):
+        self.stream = stream
+        self.total_ms = 0.0
+        self.launches = 0
+
+    def __enter__(self):
+        _check(lib().c128_kernel_timer_begin(_stream_handle(self.stream)), "c128_kernel_timer_begin")
+        return self
+
+    def __exit__(self, *exc):
+        ms, n = ctypes.c_double(0), ctypes.c_int64(0)
+        _check(lib().c128_kernel_timer_end(_stream_handle(self.stream), ctypes.byref(ms), ctypes.byref(n)),
+               "c128_kernel_timer_end")
+        self.total_ms, self.launches = ms.value, n.value
+        return False
+
+
+def info() -> dict:
+    i = Info()
+    _check(lib().c128_get_info(ctypes.byref(i)), "c128_get_info")
+    return {f: getattr(i, f) for f, _ in Info._fields_}
+
+
+def release_all() -> None:
+    _check(lib().c128_release_all(), "c128_release_all")

@@ -1,0 +1,75 @@
+// Internal declarations shared by the kernel translation unit and the C-ABI layer.
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace c128 {
+
+// C128 layout (vLLM PR #44230, Summary; fused_compress_quant_cache API page, constexprs of
+// _fused_kv_compress_norm_rope_insert_sparse_attn).
+constexpr int kHead = 512;          // head size = state width
+constexpr int kRow = 1024;          // fp32 values per state row: kv[512] | score[512]
+constexpr int kStateBlock = 8;      // rows per state-cache block
+constexpr int kRatio = 128;         // compress ratio = rows per window
+constexpr int kWindowBlocks = kRatio / kStateBlock;  // 16
+constexpr int kNope = 448;
+constexpr int kRope = 64;
+constexpr int kQuantBlock = 64;
+constexpr int kTokenStride = 576;   // bytes: 448 e4m3 + 64 bf16
+constexpr int kScaleDim = 8;        // 7 UE8M0 bytes + 1 zero pad
+constexpr int kSlotBytes = kTokenStride + kScaleDim;  // 584
+
+// Compress-kernel geometry.
+constexpr int kStages = 6;                         // smem ring depth, one state block per stage
+constexpr int kStageBytes = kStateBlock * kRow * 4;  // 32 KiB
+constexpr int kDescSlots = 2;                      // windows in flight per CTA
+constexpr int kConsumerWarps = 8;                  // warp w owns columns [64w, 64w+64)
+constexpr int kThreads = 64 + 32 * kConsumerWarps;  // scheduler warp, copy warp, consumers
+constexpr int kPlanThreads = 256;
+constexpr int kPlanTokensPerThread = 8;
+constexpr int kPlanTokensPerCta = kPlanThreads * kPlanTokensPerThread;
+constexpr unsigned long long kWaitTimeoutNs = 1000ull * 1000ull * 1000ull;  // 1 s per wait
+
+// Workspace layout: a 256-byte header then the list of active token indices.
+struct WsHeader {
+  unsigned int count;   // active windows found by the planning kernel (zeroed per call)
+  unsigned int next;    // next window to claim (zeroed per call)
+  unsigned int err;     // sticky C128_DEV_* bits
+  unsigned int pad[61];
+};
+static_assert(sizeof(WsHeader) == 256, "workspace header is 256 bytes");
+
+struct Params {
+  const int32_t* ttr;
+  const int64_t* pos;
+  const int64_t* slot;
+  const int64_t* kvslot;
+  int64_t T;
+  const int32_t* bt;
+  int64_t bt_rows, bt_cols, bt_stride;
+  const float* state;
+  int64_t nb, s0, s1;         // blocks, strides in elements
+  const float* rms_w;
+  float eps;
+  const float* cs;
+  int64_t cs_rows, cs_stride;
+  uint8_t* kc;
+  int64_t nkb, kv_bs, kc_stride0;  // blocks, block size, block stride in bytes
+  float* comp_out;            // nullable [T, 512]
+  WsHeader* ws;               // header; the token list follows it
+};
+
+struct LaunchCfg {
+  int sm_count;
+  int grid;
+  bool pdl;
+  cudaEvent_t ev_begin;  // recorded around the compress kernel when non-null
+  cudaEvent_t ev_end;
+};
+
+// Enqueue zeroing of the per-call counters, the planning kernel and the compress kernel.
+cudaError_t launch(const Params& p, const LaunchCfg& cfg, cudaStream_t stream);
+int compress_smem_bytes();
+cudaError_t prepare_device(int device);  // one-time function attributes
+
+}  // namespace c128

@@ -65,7 +65,7 @@ class Problem:
 
     @property
     def num_blocks(self) -> int:
-        return int(self.state.shape[0])
+        return int(self.state.shape[0]) if self.state is not None else 0
 
 
 def _cos_sin_cache(max_pos: int, theta: float = 10000.0) -> np.ndarray:
@@ -85,7 +85,10 @@ def _draw_state_numpy(rng: np.random.Generator, num_blocks: int) -> np.ndarray:
 
 
 def draw_state(seed: int, num_blocks: int, device: str = "cpu"):
-    """State cache ``[num_blocks, 8, 1024]``: kv ~ N(0,1) then score ~ N(0,2) in every row."""
+    """State cache ``[num_blocks, 8, 1024]``: kv ~ N(0,1) then score ~ N(0,2) in every row.
+    ``device="none"`` skips the draw (metadata-only problems)."""
+    if device == "none":
+        return None
     if device == "cpu":
         return _draw_state_numpy(np.random.default_rng([seed, 0x5EED]), num_blocks)
     import torch

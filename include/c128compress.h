@@ -1,0 +1,197 @@
+/*
+ * libc128compress — GB300 (sm_103a) DeepSeek-V4 C128 sparse-attention KV compressor.
+ *
+ * One stream-ordered call, compress_norm_rope_store(), does for every active token
+ *   1. window gather: the 128 state-cache rows p-127 .. p of the token's request, found through
+ *      the paged block table (state block size 8, so 16 whole blocks);
+ *   2. a per-column softmax of score (row columns 512..1023) over those 128 rows and the
+ *      softmax-weighted sum of kv (row columns 0..511): compressed[512], fp32;
+ *   3. RMSNorm with weight rms_w and eps;
+ *   4. FP8 e4m3 quantisation of the 448 "nope" columns with one UE8M0 (power-of-two) scale per
+ *      64 columns, and interleaved-pair (GPT-J) RoPE of the 64 rope columns, stored as bf16;
+ *   5. the paged k_cache store at kv_slot_mapping[t].
+ * It follows the fused Triton kernel _fused_kv_compress_norm_rope_insert_sparse_attn and its
+ * launcher compress_norm_rope_store_triton on the API page of
+ * vllm.models.deepseek_v4.common.ops.fused_compress_quant_cache (sections "Gather state cache
+ * entries", "Softmax + weighted sum", "RMSNorm", "KV cache pointers", "FP8 UE8M0 quant",
+ * "GPT-J RoPE"), in the C128 layout of vLLM PR #44230 "optimize the compressor 128 split cutedsl
+ * kernel" (Summary: head 512, state width 512, compress ratio 128, no overlap, state block 8;
+ * Changes: reject unsupported layouts and kv_cache_block_size != k_cache.shape[1]).
+ *
+ * Arithmetic (where the pages leave precision open): the softmax and weighted sum run in fp32
+ * (within 1e-5 relative / 1e-6 absolute of the exact value); from compressed[] on, every step is
+ * a fixed IEEE computation, so the bytes are a pure function of compressed[]:
+ *   var = RN32(exact(sum c^2) / 512); rrms = RN32(1 / sqrt(double(RN32(var + eps))));
+ *   normed = RN32(RN32(c * rrms) * w); nope: bf16 round, absmax (floor RN32(1e-4)),
+ *   e = ceil(log2(RN32(absmax * RN32(1/448)))), q = e4m3_rn_satfinite(clamp(x * 2^-e, +-448)),
+ *   scale byte = clamp(e + 127, 0, 255), 8th scale byte 0; rope: e' = RN32(RN32(e*C) - RN32(o*S)),
+ *   o' = RN32(RN32(o*C) + RN32(e*S)), each stored as bf16 (round to nearest even).
+ *
+ * A token is active iff slot_mapping[t] >= 0, positions[t] >= 0, (positions[t] + 1) % 128 == 0
+ * and kv_slot_mapping[t] >= 0. Inactive tokens write nothing; no byte of k_cache outside the
+ * 576 token bytes and 8 scale bytes of an active token's slot is touched.
+ *
+ * All tensors are caller-owned device memory described by c128_tensor_t (strides in elements).
+ * The call is asynchronous on `stream` (no host synchronisation, no device-to-host read).
+ * It uses a per-(device, stream) workspace owned by the library: the first call on a stream, and
+ * any call with more tokens than that workspace holds, allocates it with cudaMalloc (call
+ * c128_reserve_workspace first to keep later calls, for example under CUDA-graph capture, free
+ * of allocation). Calls on the same stream are serialised by the stream; calls on different
+ * streams use different workspaces. Two active tokens naming the same kv slot race (undefined
+ * which one lands); this is not checked.
+ */
+#ifndef C128COMPRESS_H
+#define C128COMPRESS_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t; 0 is the legacy default stream. */
+typedef struct CUstream_st* c128_stream_t;
+
+/* Element types of c128_tensor_t. */
+enum {
+    C128_I32 = 1,
+    C128_I64 = 2,
+    C128_F32 = 3,
+    C128_U8 = 4,
+};
+
+/* A strided view of caller-owned device memory. shape/stride beyond ndim are ignored. */
+typedef struct c128_tensor {
+    void* data;          /* device pointer (may be NULL only when the tensor is empty) */
+    int32_t dtype;       /* one of C128_I32, C128_I64, C128_F32, C128_U8 */
+    int32_t ndim;        /* 1 .. 4 */
+    int64_t shape[4];
+    int64_t stride[4];   /* in elements */
+} c128_tensor_t;
+
+/* Return codes. Every error is detected on the host before anything is launched, except
+ * C128_ERR_CUDA (a CUDA call or launch failed) and C128_ERR_NOMEM (workspace allocation). */
+enum {
+    C128_OK = 0,
+    C128_ERR_NULL_PTR = 1,     /* a descriptor, or the data of a non-empty tensor, is NULL */
+    C128_ERR_DTYPE = 2,        /* wrong element type */
+    C128_ERR_SHAPE = 3,        /* wrong rank / extent, or token counts disagree */
+    C128_ERR_STRIDE = 4,       /* innermost dimension not contiguous, or an unusable stride */
+    C128_ERR_ALIGN = 5,        /* state_cache or k_cache base/stride not aligned (see below) */
+    C128_ERR_UNSUPPORTED = 6,  /* not the C128 layout: state block != 8, row != 1024, head != 512 */
+    C128_ERR_ARG = 7,          /* kv_block_size < 1 or != k_cache.shape[1]; too many tokens */
+    C128_ERR_CUDA = 8,
+    C128_ERR_NOMEM = 9,
+};
+
+/* Device-side error bits (OR-ed into the stream's workspace, sticky until cleared).
+ * An active token whose indices fall outside the given tensors is skipped (writes nothing)
+ * and reports one of the first five bits; a bounded wait that ran out reports TIMEOUT. */
+enum {
+    C128_DEV_BAD_REQ = 1,        /* token_to_req_indices[t] outside [0, block_table.shape[0]) */
+    C128_DEV_BAD_BT_COL = 2,     /* positions[t] / 8 >= block_table.shape[1] */
+    C128_DEV_BAD_BLOCK = 4,      /* a window block id outside [0, state_cache.shape[0]) */
+    C128_DEV_BAD_COS_ROW = 8,    /* window start (p/128)*128 >= cos_sin_cache.shape[0] */
+    C128_DEV_BAD_KV_SLOT = 16,   /* kv_slot_mapping[t] >= k_cache.shape[0] * kv_block_size */
+    C128_DEV_TIMEOUT = 32,       /* a pipeline wait exceeded its time limit; the kernel gave up */
+};
+
+/*
+ * compress_norm_rope_store — the whole C128 compressor path for one batch of tokens.
+ *
+ *   token_to_req_indices [T]               int32  request of each token (contiguous)
+ *   positions            [T]               int64  absolute position of each token (contiguous)
+ *   slot_mapping         [T]               int64  state-cache slot; < 0 marks a padded token
+ *   block_table          [R, MB]           int32  state-cache block ids per request; row stride
+ *                                                 stride[0] >= MB, stride[1] == 1
+ *   state_cache          [NB, 8, 1024]     fp32   row = kv[0:512] | score[512:1024];
+ *                                                 stride[2] == 1, stride[1] >= 1024,
+ *                                                 data 16-byte aligned, stride[0] and stride[1]
+ *                                                 multiples of 4 elements
+ *   rms_w                [512]             fp32   RMSNorm weight (contiguous)
+ *   eps                                    fp32   RMSNorm epsilon
+ *   cos_sin_cache        [MP, 64]          fp32   cos in [0, 32), sin in [32, 64) of row
+ *                                                 (p / 128) * 128; stride[1] == 1
+ *   k_cache              [NKB, bs, W>=584] uint8  written in place: block b holds bs token
+ *                                                 records of 576 bytes (448 e4m3 + 64 bf16 rope)
+ *                                                 at b*stride[0] + off*576, then bs x 8 scale
+ *                                                 bytes (7 UE8M0 + a zero pad) at
+ *                                                 b*stride[0] + bs*576 + off*8; W*bs >= bs*584,
+ *                                                 data 16-byte aligned, stride[0] a multiple of 8
+ *   kv_slot_mapping      [T]               int64  k_cache slot (block*bs + offset); < 0: no store
+ *   kv_block_size                                 must equal k_cache.shape[1]
+ *   stream                                        CUDA stream the work is enqueued on
+ *
+ * Returns C128_OK or a C128_ERR_* code (nothing is launched on an error). T == 0 is a no-op.
+ */
+int compress_norm_rope_store(const c128_tensor_t* token_to_req_indices,
+                             const c128_tensor_t* positions,
+                             const c128_tensor_t* slot_mapping,
+                             const c128_tensor_t* block_table,
+                             const c128_tensor_t* state_cache,
+                             const c128_tensor_t* rms_w,
+                             float eps,
+                             const c128_tensor_t* cos_sin_cache,
+                             const c128_tensor_t* k_cache,
+                             const c128_tensor_t* kv_slot_mapping,
+                             int64_t kv_block_size,
+                             c128_stream_t stream);
+
+/*
+ * Same as compress_norm_rope_store, and also writes the fp32 compressed vector (the softmax-
+ * weighted sum, before RMSNorm) of every token it stores to comp_out [T, 512] fp32 (contiguous,
+ * 8-byte aligned). Rows of other tokens are left as they were. For tests and diagnostics: it
+ * exposes the quantity the byte-exact epilogue is a function of.
+ */
+int c128_compress_norm_rope_store_debug(const c128_tensor_t* token_to_req_indices,
+                                        const c128_tensor_t* positions,
+                                        const c128_tensor_t* slot_mapping,
+                                        const c128_tensor_t* block_table,
+                                        const c128_tensor_t* state_cache,
+                                        const c128_tensor_t* rms_w,
+                                        float eps,
+                                        const c128_tensor_t* cos_sin_cache,
+                                        const c128_tensor_t* k_cache,
+                                        const c128_tensor_t* kv_slot_mapping,
+                                        int64_t kv_block_size,
+                                        const c128_tensor_t* comp_out,
+                                        c128_stream_t stream);
+
+/* Human-readable name of a return code (static string, never NULL). */
+const char* c128_status_string(int status);
+
+/* Make the workspace of (current device, stream) hold at least max_tokens tokens. May call
+ * cudaMalloc/cudaFree (and synchronise the stream when it replaces a smaller workspace). */
+int c128_reserve_workspace(int64_t max_tokens, c128_stream_t stream);
+
+/* Synchronise `stream`, store the device error bits (C128_DEV_*) of its workspace in *bits,
+ * and clear them when `clear` is non-zero. A stream never used reports 0. */
+int c128_device_errors(c128_stream_t stream, uint32_t* bits, int clear);
+
+/* Kernel timer. Between begin and end, every call on `stream` records a CUDA event pair around
+ * its compress kernel (the dominant kernel; the planning kernel is outside the pair). end()
+ * synchronises the stream and returns the summed kernel time in ms and the number of launches.
+ * While the timer runs the compress kernel does not overlap the planning kernel. */
+int c128_kernel_timer_begin(c128_stream_t stream);
+int c128_kernel_timer_end(c128_stream_t stream, double* total_ms, int64_t* launches);
+
+/* Static launch facts of the compress kernel on the current device. */
+typedef struct c128_info {
+    int32_t sm_count;        /* streaming multiprocessors */
+    int32_t threads;         /* threads per CTA of the compress kernel */
+    int32_t smem_bytes;      /* dynamic shared memory per CTA */
+    int32_t stages;          /* shared-memory ring depth, 32 KiB (one state block) per stage */
+    int32_t ctas_per_sm;     /* resident CTAs per SM */
+    int32_t plan_tokens_per_cta;
+    int32_t wait_timeout_ms; /* limit of every pipeline wait */
+    int32_t version;
+} c128_info_t;
+int c128_get_info(c128_info_t* info);
+
+/* Free every workspace and timer the library holds (synchronises the device). */
+int c128_release_all(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* C128COMPRESS_H */

@@ -1,0 +1,183 @@
+"""Host-only checks of the C-ABI library (no GPU needed): it builds for sm_103a, loads, exports
+every function include/c128compress.h declares, and rejects bad arguments before touching CUDA.
+Also checks that the CUDA path and the oracle share no code."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+from deepseek_v4_sparse_c128_gb300 import binding, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "c128compress.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    build.build()
+    return binding.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b([a-z_][a-z0-9_]*)\s*\(", text, flags=re.M))
+                  - {"if", "while", "for", "return", "sizeof"})
+
+
+def test_header_declarations_are_exported(L):
+    names = declared_functions()
+    assert "compress_norm_rope_store" in names
+    assert sorted(binding.EXPORTS) == names
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def test_symbols_visible_to_nm():
+    import subprocess
+    out = subprocess.run(["nm", "-D", "--defined-only", build.LIB], capture_output=True, text=True).stdout
+    syms = {line.split()[-1] for line in out.splitlines() if line.strip()}
+    for n in declared_functions():
+        assert n in syms, n
+
+
+def test_status_strings(L):
+    for code in range(0, 10):
+        s = L.c128_status_string(code)
+        assert s and s != b"unknown status", code
+    assert L.c128_status_string(99) == b"unknown status"
+
+
+FAKE = 1 << 20  # an aligned address that validation never dereferences
+
+
+def _t(shape, dtype, data=FAKE, strides=None):
+    d = binding.Tensor()
+    d.data = data
+    d.dtype = dtype
+    d.ndim = len(shape)
+    if strides is None:
+        strides, acc = [], 1
+        for n in reversed(shape):
+            strides.insert(0, acc)
+            acc *= n
+    for i, (n, s) in enumerate(zip(shape, strides)):
+        d.shape[i], d.stride[i] = n, s
+    return d
+
+
+def _args(T=0, **over):
+    I32, I64, F32, U8 = binding.C128_I32, binding.C128_I64, binding.C128_F32, binding.C128_U8
+    a = dict(ttr=_t([T], I32), pos=_t([T], I64), slot=_t([T], I64), bt=_t([4, 64], I32),
+             state=_t([64, 8, 1024], F32), rms=_t([512], F32), eps=1e-6, cs=_t([512, 64], F32),
+             kc=_t([4, 2, 584], U8), kvs=_t([T], I64), bs=2)
+    a.update(over)
+    return a
+
+
+def _call(L, a):
+    r = lambda x: ctypes.byref(x) if x is not None else None
+    return L.compress_norm_rope_store(r(a["ttr"]), r(a["pos"]), r(a["slot"]), r(a["bt"]), r(a["state"]),
+                                      r(a["rms"]), ctypes.c_float(a["eps"]), r(a["cs"]), r(a["kc"]), r(a["kvs"]),
+                                      a["bs"], None)
+
+
+def test_empty_call_is_ok_without_gpu(L):
+    assert _call(L, _args(T=0)) == 0
+
+
+@pytest.mark.parametrize("case,code", [
+    ("null_desc", 1), ("null_data", 1), ("pos_dtype", 2), ("state_dtype", 2), ("kc_dtype", 2),
+    ("T_mismatch", 3), ("state_rank", 3), ("kc_width", 3), ("pos_stride", 4), ("state_inner_stride", 4),
+    ("kc_inner", 4), ("state_misaligned", 5), ("state_stride_odd", 5), ("kc_stride0", 5),
+    ("block8", 6), ("row1024", 6), ("head512", 6), ("rope64", 6), ("bs_mismatch", 7), ("bs_zero", 7),
+])
+def test_validation_codes(L, case, code):
+    I32, I64, F32, U8 = binding.C128_I32, binding.C128_I64, binding.C128_F32, binding.C128_U8
+    T = 5
+    a = _args(T=T)
+    if case == "null_desc":
+        a["bt"] = None
+    elif case == "null_data":
+        a["slot"] = _t([T], I64, data=None)
+    elif case == "pos_dtype":
+        a["pos"] = _t([T], I32)
+    elif case == "state_dtype":
+        a["state"] = _t([64, 8, 1024], U8)
+    elif case == "kc_dtype":
+        a["kc"] = _t([4, 2, 584], I32)
+    elif case == "T_mismatch":
+        a["kvs"] = _t([T + 1], I64)
+    elif case == "state_rank":
+        a["state"] = _t([64, 8192], F32)
+    elif case == "kc_width":
+        a["kc"] = _t([4, 2, 583], U8)
+    elif case == "pos_stride":
+        a["pos"] = _t([T], I64, strides=[2])
+    elif case == "state_inner_stride":
+        a["state"] = _t([64, 8, 1024], F32, strides=[16384, 2048, 2])
+    elif case == "kc_inner":
+        a["kc"] = _t([4, 2, 584], U8, strides=[1168, 584, 2])
+    elif case == "state_misaligned":
+        a["state"] = _t([64, 8, 1024], F32, data=FAKE + 4)
+    elif case == "state_stride_odd":
+        a["state"] = _t([64, 8, 1024], F32, strides=[8 * 1026, 1026, 1])
+    elif case == "kc_stride0":
+        a["kc"] = _t([4, 1, 584], U8, strides=[588, 584, 1])
+        a["bs"] = 1
+    elif case == "block8":
+        a["state"] = _t([64, 16, 1024], F32)
+    elif case == "row1024":
+        a["state"] = _t([64, 8, 2048], F32)
+    elif case == "head512":
+        a["rms"] = _t([128], F32)
+    elif case == "rope64":
+        a["cs"] = _t([512, 32], F32)
+    elif case == "bs_mismatch":
+        a["bs"] = 4
+    elif case == "bs_zero":
+        a["bs"] = 0
+    assert _call(L, a) == code
+
+
+def test_debug_entry_requires_comp_out(L):
+    a = _args(T=0)
+    r = ctypes.byref
+    rc = L.c128_compress_norm_rope_store_debug(r(a["ttr"]), r(a["pos"]), r(a["slot"]), r(a["bt"]), r(a["state"]),
+                                               r(a["rms"]), ctypes.c_float(1e-6), r(a["cs"]), r(a["kc"]),
+                                               r(a["kvs"]), 2, None, None)
+    assert rc == 1
+    comp = _t([0, 512], binding.C128_F32)
+    rc = L.c128_compress_norm_rope_store_debug(r(a["ttr"]), r(a["pos"]), r(a["slot"]), r(a["bt"]), r(a["state"]),
+                                               r(a["rms"]), ctypes.c_float(1e-6), r(a["cs"]), r(a["kc"]),
+                                               r(a["kvs"]), 2, r(comp), None)
+    assert rc == 0
+
+
+def _sources(folder, exts):
+    for dp, _, fs in os.walk(os.path.join(ROOT, folder)):
+        for f in fs:
+            if f.endswith(exts):
+                yield os.path.join(dp, f)
+
+
+def test_oracle_and_cuda_path_share_no_code():
+    pkg = "deepseek_v4_sparse_c128_gb300"
+    for f in _sources(pkg, (".py", ".cu", ".h", ".cuh", ".cpp")):
+        text = open(f).read()
+        assert not re.search(r"^\s*(import|from)\s+oracle\b", text, flags=re.M), f
+        assert "c128_oracle" not in text and "libc128oracle" not in text, f
+    for f in _sources("oracle", (".py", ".c", ".h")):
+        text = open(f).read()
+        assert "csrc" not in text and "libc128compress" not in text, f
+        assert not re.search(r"^\s*(import|from)\s+deepseek_v4_sparse_c128_gb300\.(binding|build)", text, flags=re.M), f
+        assert not re.search(r"#include\s+\"[^\"]*c128(compress|_internal)", text), f
+
+
+def test_inputs_module_holds_no_method_arithmetic():
+    text = open(os.path.join(ROOT, "deepseek_v4_sparse_c128_gb300", "inputs.py")).read()
+    for word in ("softmax", "np.exp", "rsqrt", "sqrt", "e4m3", "bfloat16", "float8", "log2", "ceil("):
+        assert word not in text, word
+    assert np is not None
