@@ -40,7 +40,7 @@ STATE_BYTES_PER_WINDOW = 128 * 1024 * 4                       # 524,288
 ALGO_BYTES_PER_WINDOW = STATE_BYTES_PER_WINDOW + 64 + 256 + 584  # + block ids, cos/sin row, k_cache write
 PAGES_US_16374 = 1425.900  # vLLM PR #44230, Performance table (B300), token_num 16374
 KERNEL_SRC = os.path.join(ROOT, "deepseek_v4_sparse_c128_gb300", "csrc", "c128_kernels.cu")
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "compress_kernel_traffic.json")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "compress_kernel_sweep1024_traffic.json")
 
 
 def workload_config(T: int, n_gpus: int) -> dict:
@@ -232,30 +232,36 @@ def run_ours(args, ws, rank, local):
     kernel_ms = ktimer.total_ms / max(1, ktimer.launches)
 
     # ---- end to end through the public API: per-step metadata from pinned host memory in, k_cache out
-    host = {k: torch.from_numpy(np.ascontiguousarray(getattr(p, k))).pin_memory()
-            for k in ("token_to_req", "positions", "slot_mapping", "block_table", "kv_slot_mapping")}
-    kc_host = torch.empty(d["k_cache"].shape, dtype=torch.uint8).pin_memory()
-    h2d = sum(int(v.numel() * v.element_size()) for v in host.values())
-    d2h = int(kc_host.numel())
+    e2e = None
+    if not args.no_e2e:
+        host = {k: torch.from_numpy(np.ascontiguousarray(getattr(p, k))).pin_memory()
+                for k in ("token_to_req", "positions", "slot_mapping", "block_table", "kv_slot_mapping")}
+        kc_host = torch.empty(d["k_cache"].shape, dtype=torch.uint8).pin_memory()
+        h2d = sum(int(v.numel() * v.element_size()) for v in host.values())
+        d2h = int(kc_host.numel())
 
-    def e2e_step():
-        for k, v in host.items():
-            d[k].copy_(v, non_blocking=True)
-        step()
-        kc_host.copy_(d["k_cache"], non_blocking=True)
+        def e2e_step():
+            for k, v in host.items():
+                d[k].copy_(v, non_blocking=True)
+            step()
+            kc_host.copy_(d["k_cache"], non_blocking=True)
 
-    e2e_steps = max(3, min(args.steps, 200))
-    for _ in range(3):
-        e2e_step()
-    torch.cuda.synchronize()
-    barrier(ws)
-    t0 = time.perf_counter()
-    for _ in range(e2e_steps):
-        e2e_step()
-    torch.cuda.synchronize()
-    e2e_s = time.perf_counter() - t0
-    barrier(ws)
-    e2e_max_ms, e2e_windows = reduce_max_sum(ws, e2e_s * 1e3, float(T * e2e_steps))
+        e2e_steps = max(3, min(args.steps, 200))
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize()
+        barrier(ws)
+        t0 = time.perf_counter()
+        for _ in range(e2e_steps):
+            e2e_step()
+        torch.cuda.synchronize()
+        e2e_s = time.perf_counter() - t0
+        barrier(ws)
+        e2e_max_ms, e2e_windows = reduce_max_sum(ws, e2e_s * 1e3, float(T * e2e_steps))
+        e2e = {"value": e2e_windows / (e2e_max_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+               "note": "state cache resident (it is a cache); per-step token metadata and block table in, "
+                       "whole k_cache out"}
 
     out = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
@@ -265,10 +271,7 @@ def run_ours(args, ws, rank, local):
            "us_per_call": ms_per_step * 1e3,
            "hbm_gbs_per_gpu": T * ALGO_BYTES_PER_WINDOW / (ms_per_step * 1e-3) / 1e9,
            "gpu_launches": 2 * args.steps}
-    out["e2e"] = {"value": e2e_windows / (e2e_max_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
-                  "d2h_bytes_per_step": d2h, "steps": e2e_steps,
-                  "note": "state cache resident (it is a cache); per-step token metadata and block table in, "
-                          "whole k_cache out"}
+    out["e2e"] = e2e
     peaks = {}
     try:
         peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
@@ -390,6 +393,7 @@ def main():
     ap.add_argument("--tokens", type=int, default=HEADLINE_T)
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
     args = ap.parse_args()
     ws, rank, local = dist_setup()
     try:
