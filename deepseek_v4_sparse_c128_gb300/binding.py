@@ -17,13 +17,16 @@ C128_I32, C128_I64, C128_F32, C128_U8 = 1, 2, 3, 4
 STATUS = {
     0: "C128_OK", 1: "C128_ERR_NULL_PTR", 2: "C128_ERR_DTYPE", 3: "C128_ERR_SHAPE", 4: "C128_ERR_STRIDE",
     5: "C128_ERR_ALIGN", 6: "C128_ERR_UNSUPPORTED", 7: "C128_ERR_ARG", 8: "C128_ERR_CUDA", 9: "C128_ERR_NOMEM",
+    10: "C128_ERR_TOO_MANY_TOKENS",
 }
+NOALLOC_MAX_TOKENS = 65536  # C128_NOALLOC_MAX_TOKENS
 DEV_BITS = {1: "BAD_REQ", 2: "BAD_BT_COL", 4: "BAD_BLOCK", 8: "BAD_COS_ROW", 16: "BAD_KV_SLOT", 32: "TIMEOUT"}
 
 # Every entry point the header declares, with its ctypes signature.
 EXPORTS = (
     "compress_norm_rope_store",
     "c128_compress_norm_rope_store_debug",
+    "c128_compress_norm_rope_store_noalloc",
     "c128_status_string",
     "c128_reserve_workspace",
     "c128_device_errors",
@@ -72,6 +75,7 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     i64, vp = ctypes.c_int64, ctypes.c_void_p
     L.compress_norm_rope_store.argtypes = [T, T, T, T, T, T, ctypes.c_float, T, T, T, i64, vp]
     L.c128_compress_norm_rope_store_debug.argtypes = [T, T, T, T, T, T, ctypes.c_float, T, T, T, i64, T, vp]
+    L.c128_compress_norm_rope_store_noalloc.argtypes = [T, T, T, T, T, T, ctypes.c_float, T, T, T, i64, vp]
     L.c128_status_string.argtypes = [ctypes.c_int]
     L.c128_status_string.restype = ctypes.c_char_p
     L.c128_reserve_workspace.argtypes = [i64, vp]
@@ -152,6 +156,21 @@ def compress_norm_rope_store(token_to_req_indices, positions, slot_mapping, bloc
         rc = L.c128_compress_norm_rope_store_debug(*refs, ctypes.c_float(eps), ctypes.byref(cs), ctypes.byref(kc),
                                                    ctypes.byref(kvs), int(kv_block_size), ctypes.byref(co), h)
         _check(rc, "c128_compress_norm_rope_store_debug")
+
+
+def compress_norm_rope_store_noalloc(token_to_req_indices, positions, slot_mapping, block_table, state_cache,
+                                     rms_w, eps: float, cos_sin_cache, k_cache, kv_slot_mapping,
+                                     kv_block_size: int, stream=None) -> None:
+    """The entry point that allocates no device memory (its scratch is a static device array of
+    NOALLOC_MAX_TOKENS tokens); same arguments and results as compress_norm_rope_store. For
+    callers that must not allocate once running. Calls that overlap on the GPU race."""
+    L = lib()
+    descs = [describe(x) for x in (token_to_req_indices, positions, slot_mapping, block_table, state_cache, rms_w)]
+    cs, kc, kvs = describe(cos_sin_cache), describe(k_cache), describe(kv_slot_mapping)
+    rc = L.c128_compress_norm_rope_store_noalloc(*[ctypes.byref(a) for a in descs], ctypes.c_float(eps),
+                                                 ctypes.byref(cs), ctypes.byref(kc), ctypes.byref(kvs),
+                                                 int(kv_block_size), _stream_handle(stream))
+    _check(rc, "c128_compress_norm_rope_store_noalloc")
 
 
 def call_status(*args, **kw) -> int:

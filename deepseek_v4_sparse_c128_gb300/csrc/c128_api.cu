@@ -122,10 +122,10 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
     if (rc_ != C128_OK) return rc_; \
   } while (0)
 
-int run(const c128_tensor_t* ttr, const c128_tensor_t* pos, const c128_tensor_t* slot,
-        const c128_tensor_t* bt, const c128_tensor_t* state, const c128_tensor_t* rms_w, float eps,
-        const c128_tensor_t* cs, const c128_tensor_t* kc, const c128_tensor_t* kvslot,
-        int64_t kv_block_size, const c128_tensor_t* comp_out, cudaStream_t stream) {
+int validate_call(const c128_tensor_t* ttr, const c128_tensor_t* pos, const c128_tensor_t* slot,
+                  const c128_tensor_t* bt, const c128_tensor_t* state, const c128_tensor_t* rms_w, float eps,
+                  const c128_tensor_t* cs, const c128_tensor_t* kc, const c128_tensor_t* kvslot,
+                  int64_t kv_block_size, const c128_tensor_t* comp_out, c128::Params* out) {
   // per-token vectors (the pages' token_to_req_indices, positions, slot_mapping, kv slot map)
   if (pos == nullptr) return C128_ERR_NULL_PTR;
   C128_TRY(check_desc(pos, C128_I64, 1));
@@ -175,11 +175,45 @@ int run(const c128_tensor_t* ttr, const c128_tensor_t* pos, const c128_tensor_t*
     C128_TRY(check_data(comp_out));
     if (!aligned(comp_out->data, 8)) return C128_ERR_ALIGN;
   }
+  c128::Params& p = *out;
+  p = c128::Params{};
+  p.ttr = static_cast<const int32_t*>(ttr->data);
+  p.pos = static_cast<const int64_t*>(pos->data);
+  p.slot = static_cast<const int64_t*>(slot->data);
+  p.kvslot = static_cast<const int64_t*>(kvslot->data);
+  p.T = T;
+  p.bt = static_cast<const int32_t*>(bt->data);
+  p.bt_rows = bt->shape[0];
+  p.bt_cols = bt->shape[1];
+  p.bt_stride = bt->shape[0] > 1 ? bt->stride[0] : bt->shape[1];
+  p.state = static_cast<const float*>(state->data);
+  p.nb = state->shape[0];
+  p.s0 = state->stride[0];
+  p.s1 = state->stride[1];
+  p.rms_w = static_cast<const float*>(rms_w->data);
+  p.eps = eps;
+  p.cs = static_cast<const float*>(cs->data);
+  p.cs_rows = cs->shape[0];
+  p.cs_stride = cs->shape[0] > 1 ? cs->stride[0] : c128::kRope;
+  p.kc = static_cast<uint8_t*>(kc->data);
+  p.nkb = kc->shape[0];
+  p.kv_bs = kv_block_size;
+  p.kc_stride0 = kc->shape[0] > 1 ? kc->stride[0] : kc->shape[1] * kc->shape[2];
+  p.comp_out = comp_out != nullptr ? static_cast<float*>(comp_out->data) : nullptr;
+  return C128_OK;
+}
+
+int run(const c128_tensor_t* ttr, const c128_tensor_t* pos, const c128_tensor_t* slot,
+        const c128_tensor_t* bt, const c128_tensor_t* state, const c128_tensor_t* rms_w, float eps,
+        const c128_tensor_t* cs, const c128_tensor_t* kc, const c128_tensor_t* kvslot,
+        int64_t kv_block_size, const c128_tensor_t* comp_out, cudaStream_t stream) {
+  c128::Params p{};
+  C128_TRY(validate_call(ttr, pos, slot, bt, state, rms_w, eps, cs, kc, kvslot, kv_block_size, comp_out, &p));
+  const int64_t T = p.T;
   if (T == 0) return C128_OK;
 
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return C128_ERR_CUDA;
-  c128::Params p{};
   c128::LaunchCfg cfg{};
   {
     std::lock_guard<std::mutex> lk(g_mu);
@@ -204,34 +238,20 @@ int run(const c128_tensor_t* ttr, const c128_tensor_t* pos, const c128_tensor_t*
       ++tm.used;
     }
   }
-  p.ttr = static_cast<const int32_t*>(ttr->data);
-  p.pos = static_cast<const int64_t*>(pos->data);
-  p.slot = static_cast<const int64_t*>(slot->data);
-  p.kvslot = static_cast<const int64_t*>(kvslot->data);
-  p.T = T;
-  p.bt = static_cast<const int32_t*>(bt->data);
-  p.bt_rows = bt->shape[0];
-  p.bt_cols = bt->shape[1];
-  p.bt_stride = bt->shape[0] > 1 ? bt->stride[0] : bt->shape[1];
-  p.state = static_cast<const float*>(state->data);
-  p.nb = state->shape[0];
-  p.s0 = state->stride[0];
-  p.s1 = state->stride[1];
-  p.rms_w = static_cast<const float*>(rms_w->data);
-  p.eps = eps;
-  p.cs = static_cast<const float*>(cs->data);
-  p.cs_rows = cs->shape[0];
-  p.cs_stride = cs->shape[0] > 1 ? cs->stride[0] : c128::kRope;
-  p.kc = static_cast<uint8_t*>(kc->data);
-  p.nkb = kc->shape[0];
-  p.kv_bs = kv_block_size;
-  p.kc_stride0 = kc->shape[0] > 1 ? kc->stride[0] : kc->shape[1] * kc->shape[2];
-  p.comp_out = comp_out != nullptr ? static_cast<float*>(comp_out->data) : nullptr;
   const cudaError_t e = c128::launch(p, cfg, stream);
   return e == cudaSuccess ? C128_OK : cuda_fail(e);
 }
 
 }  // namespace
+
+namespace c128 {
+int validate_args(const c128_tensor_t* ttr, const c128_tensor_t* pos, const c128_tensor_t* slot,
+                  const c128_tensor_t* bt, const c128_tensor_t* state, const c128_tensor_t* rms_w, float eps,
+                  const c128_tensor_t* cs, const c128_tensor_t* kc, const c128_tensor_t* kvslot,
+                  int64_t kv_block_size, const c128_tensor_t* comp_out, Params* out) {
+  return validate_call(ttr, pos, slot, bt, state, rms_w, eps, cs, kc, kvslot, kv_block_size, comp_out, out);
+}
+}  // namespace c128
 
 extern "C" {
 
@@ -271,6 +291,9 @@ const char* c128_status_string(int status) {
     case C128_ERR_ARG: return "bad argument (kv_block_size must equal k_cache.shape[1]; too many tokens)";
     case C128_ERR_CUDA: return "CUDA error";
     case C128_ERR_NOMEM: return "workspace allocation failed";
+    case C128_ERR_TOO_MANY_TOKENS:
+      return "more tokens than the static workspace of c128_compress_norm_rope_store_noalloc holds "
+             "(C128_NOALLOC_MAX_TOKENS)";
     default: return "unknown status";
   }
 }

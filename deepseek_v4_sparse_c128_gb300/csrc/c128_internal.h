@@ -3,6 +3,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "c128compress.h"
+
 namespace c128 {
 
 // C128 layout (vLLM PR #44230, Summary; fused_compress_quant_cache API page, constexprs of
@@ -66,6 +68,12 @@ struct LaunchCfg {
   cudaEvent_t ev_begin;  // recorded around the compress kernel when non-null
   cudaEvent_t ev_end;
 };
+
+// Check every argument of compress_norm_rope_store (C128_* code) and fill all of `out` but `ws`.
+int validate_args(const c128_tensor_t* ttr, const c128_tensor_t* pos, const c128_tensor_t* slot,
+                  const c128_tensor_t* bt, const c128_tensor_t* state, const c128_tensor_t* rms_w, float eps,
+                  const c128_tensor_t* cs, const c128_tensor_t* kc, const c128_tensor_t* kvslot,
+                  int64_t kv_block_size, const c128_tensor_t* comp_out, Params* out);
 
 // Enqueue zeroing of the per-call counters, the planning kernel and the compress kernel.
 cudaError_t launch(const Params& p, const LaunchCfg& cfg, cudaStream_t stream);

@@ -82,6 +82,7 @@ enum {
     C128_ERR_ARG = 7,          /* kv_block_size < 1 or != k_cache.shape[1]; too many tokens */
     C128_ERR_CUDA = 8,
     C128_ERR_NOMEM = 9,
+    C128_ERR_TOO_MANY_TOKENS = 10, /* c128_compress_norm_rope_store_noalloc: T > C128_NOALLOC_MAX_TOKENS */
 };
 
 /* Device-side error bits (OR-ed into the stream's workspace, sticky until cleared).
@@ -156,6 +157,42 @@ int c128_compress_norm_rope_store_debug(const c128_tensor_t* token_to_req_indice
                                         int64_t kv_block_size,
                                         const c128_tensor_t* comp_out,
                                         c128_stream_t stream);
+
+/*
+ * c128_compress_norm_rope_store_noalloc — the same operation, for callers that cannot allocate.
+ * The pages have no counterpart to this entry point; it exists for the library's users.
+ *
+ * compress_norm_rope_store keeps its list of active tokens in a workspace that it allocates with
+ * cudaMalloc on the first call on a stream and whenever a larger batch arrives. Some callers may
+ * not allocate device memory once they are running: a serving engine that hands all free memory
+ * to its KV caches at start-up and must never see an allocation (or its implicit device
+ * synchronisation) on the decode path, code running inside a memory-pool or allocator callback,
+ * or a host that enforces a fixed device-memory budget. This entry point allocates nothing.
+ *
+ * Its scratch (a 256-byte header and the token list) is one static device array of
+ * C128_NOALLOC_MAX_TOKENS tokens (256 KiB + 256 B) in the library image; every GPU that loads the
+ * library holds it until the process exits. The first call on each device looks up that array's
+ * device address (cudaGetSymbolAddress, with that device current) and caches it; make that first
+ * call before any stream capture. Arguments, layout and results are exactly those of
+ * compress_norm_rope_store; T > C128_NOALLOC_MAX_TOKENS returns C128_ERR_TOO_MANY_TOKENS without
+ * launching anything. All calls share the one array: each call clears the counters it needs,
+ * and calls that can overlap on the GPU (different streams, or different host threads) race and
+ * corrupt each other's work. Device error bits of these calls are not readable through
+ * c128_device_errors (tokens with out-of-range indices are still skipped).
+ */
+#define C128_NOALLOC_MAX_TOKENS 65536
+int c128_compress_norm_rope_store_noalloc(const c128_tensor_t* token_to_req_indices,
+                                          const c128_tensor_t* positions,
+                                          const c128_tensor_t* slot_mapping,
+                                          const c128_tensor_t* block_table,
+                                          const c128_tensor_t* state_cache,
+                                          const c128_tensor_t* rms_w,
+                                          float eps,
+                                          const c128_tensor_t* cos_sin_cache,
+                                          const c128_tensor_t* k_cache,
+                                          const c128_tensor_t* kv_slot_mapping,
+                                          int64_t kv_block_size,
+                                          c128_stream_t stream);
 
 /* Human-readable name of a return code (static string, never NULL). */
 const char* c128_status_string(int status);

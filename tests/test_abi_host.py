@@ -44,7 +44,7 @@ def test_symbols_visible_to_nm():
 
 
 def test_status_strings(L):
-    for code in range(0, 10):
+    for code in range(0, 11):
         s = L.c128_status_string(code)
         assert s and s != b"unknown status", code
     assert L.c128_status_string(99) == b"unknown status"
