@@ -173,6 +173,41 @@ def compress_norm_rope_store_noalloc(token_to_req_indices, positions, slot_mappi
     _check(rc, "c128_compress_norm_rope_store_noalloc")
 
 
+class PreparedCall:
+    """compress_norm_rope_store with its descriptors built once, for repeated calls on the same
+    tensors (serving loops, benchmarks): calling the object is a single C-ABI call. The tensors
+    must stay alive and keep their storage; the stream is fixed when the object is built
+    (default: the current torch stream). ``noalloc=True`` targets
+    c128_compress_norm_rope_store_noalloc instead; ``comp_out`` targets the debug entry point."""
+
+    def __init__(self, token_to_req_indices, positions, slot_mapping, block_table, state_cache, rms_w, eps: float,
+                 cos_sin_cache, k_cache, kv_slot_mapping, kv_block_size: int, stream=None, comp_out=None,
+                 noalloc: bool = False):
+        L = lib()
+        self._keep = (token_to_req_indices, positions, slot_mapping, block_table, state_cache, rms_w, cos_sin_cache,
+                      k_cache, kv_slot_mapping, comp_out)
+        d = [describe(x) for x in (token_to_req_indices, positions, slot_mapping, block_table, state_cache, rms_w)]
+        cs, kc, kvs = describe(cos_sin_cache), describe(k_cache), describe(kv_slot_mapping)
+        self._descs = (*d, cs, kc, kvs)
+        args = [ctypes.byref(a) for a in d] + [ctypes.c_float(eps), ctypes.byref(cs), ctypes.byref(kc),
+                                               ctypes.byref(kvs), ctypes.c_int64(int(kv_block_size))]
+        if comp_out is not None:
+            self._co = describe(comp_out)
+            args.append(ctypes.byref(self._co))
+            self._fn, self._name = L.c128_compress_norm_rope_store_debug, "c128_compress_norm_rope_store_debug"
+        elif noalloc:
+            self._fn, self._name = L.c128_compress_norm_rope_store_noalloc, "c128_compress_norm_rope_store_noalloc"
+        else:
+            self._fn, self._name = L.compress_norm_rope_store, "compress_norm_rope_store"
+        args.append(ctypes.c_void_p(_stream_handle(stream)))
+        self._args = tuple(args)
+
+    def __call__(self) -> None:
+        rc = self._fn(*self._args)
+        if rc != 0:
+            raise C128Error(rc, self._name)
+
+
 def call_status(*args, **kw) -> int:
     """Like compress_norm_rope_store but returns the status code instead of raising."""
     try:

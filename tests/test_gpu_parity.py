@@ -272,6 +272,24 @@ def test_streams_graphs_and_timer():
     assert ref is not None
 
 
+def test_prepared_call_matches_function_call():
+    import torch
+    from deepseek_v4_sparse_c128_gb300 import binding
+    p = inputs.make_problem("mixed")
+    kc_ref, comp_ref, _ = run_gpu(p)
+    d = to_device(p)
+    comp = torch.zeros((p.num_tokens, 512), dtype=torch.float32, device="cuda")
+    call = binding.PreparedCall(d["token_to_req"], d["positions"], d["slot_mapping"], d["block_table"], d["state"],
+                                d["rms_w"], p.eps, d["cos_sin"], d["k_cache"], d["kv_slot_mapping"], p.kv_block_size,
+                                comp_out=comp)
+    call()
+    call()  # idempotent: same inputs, same bytes
+    torch.cuda.synchronize()
+    assert np.array_equal(d["k_cache"].cpu().numpy(), kc_ref)
+    rows = written_rows(comp_ref)
+    assert np.array_equal(comp.cpu().numpy()[rows].view(np.uint32), comp_ref[rows].view(np.uint32))
+
+
 def test_host_validation_on_gpu():
     """Layout errors are rejected before anything is launched."""
     import torch
