@@ -242,7 +242,7 @@ def run_ours(args, ws, rank, local):
             bufs[1][k].copy_(d[k])
         bufs[1]["k_cache"].copy_(d["k_cache"])
         kc_host = [torch.empty(d["k_cache"].shape, dtype=torch.uint8).pin_memory() for _ in range(2)]
-        copy_stream = torch.cuda.Stream(device=dev)
+        up_stream, down_stream = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
         calls = [binding.PreparedCall(b["token_to_req"], b["positions"], b["slot_mapping"], b["block_table"],
                                       b["state"], b["rms_w"], p.eps, b["cos_sin"], b["k_cache"], b["kv_slot_mapping"],
                                       p.kv_block_size, stream=stream) for b in bufs]
@@ -252,24 +252,30 @@ def run_ours(args, ws, rank, local):
         computed = [torch.cuda.Event() for _ in range(2)]
         read_back = [torch.cuda.Event() for _ in range(2)]
 
+        def upload(i):
+            j = i & 1
+            with torch.cuda.stream(up_stream):
+                if i >= 2:
+                    up_stream.wait_event(computed[j])           # metadata buffer j free again
+                for k in keys:
+                    bufs[j][k].copy_(host[k], non_blocking=True)
+                uploaded[j].record(up_stream)
+
         def run_e2e(n):
+            upload(0)
             for i in range(n):
                 j = i & 1
-                with torch.cuda.stream(copy_stream):
-                    if i >= 2:
-                        copy_stream.wait_event(computed[j])      # buffer j free again
-                    for k in keys:
-                        bufs[j][k].copy_(host[k], non_blocking=True)
-                    uploaded[j].record(copy_stream)
+                if i + 1 < n:
+                    upload(i + 1)                               # next step's inputs stream in meanwhile
                 stream.wait_event(uploaded[j])
                 if i >= 2:
                     stream.wait_event(read_back[j])             # k_cache j read back before reuse
                 calls[j]()
                 computed[j].record(stream)
-                with torch.cuda.stream(copy_stream):
-                    copy_stream.wait_event(computed[j])
+                with torch.cuda.stream(down_stream):
+                    down_stream.wait_event(computed[j])
                     kc_host[j].copy_(bufs[j]["k_cache"], non_blocking=True)
-                    read_back[j].record(copy_stream)
+                    read_back[j].record(down_stream)
             torch.cuda.synchronize()
 
         e2e_steps = max(3, min(args.steps, 200))
@@ -285,7 +291,7 @@ def run_ours(args, ws, rank, local):
                "d2h_bytes_per_step": d2h, "steps": e2e_steps,
                "note": "public API (binding.PreparedCall -> C-ABI) with host buffers: each step uploads token "
                        "metadata + block table from pinned memory and reads the whole k_cache back; copies on a "
-                       "side stream, double-buffered; state cache resident (it is a cache)"}
+                       "upload and read-back streams, double-buffered so both overlap the kernels; state cache resident (it is a cache)"}
 
     out = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",

@@ -22,7 +22,10 @@ constexpr int kScaleDim = 8;        // 7 UE8M0 bytes + 1 zero pad
 constexpr int kSlotBytes = kTokenStride + kScaleDim;  // 584
 
 // Compress-kernel geometry.
-constexpr int kStages = 6;                         // smem ring depth, one state block per stage
+#ifndef C128_STAGES
+#define C128_STAGES 6
+#endif
+constexpr int kStages = C128_STAGES;               // smem ring depth, one state block per stage
 constexpr int kStageBytes = kStateBlock * kRow * 4;  // 32 KiB
 constexpr int kDescSlots = 2;                      // windows in flight per CTA
 constexpr int kConsumerWarps = 8;                  // warp w owns columns [64w, 64w+64)

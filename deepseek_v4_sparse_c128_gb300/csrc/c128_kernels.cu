@@ -67,9 +67,17 @@ __device__ __noinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const vol
     if (global_timer_ns() - t0 > kWaitTimeoutNs) return false;
   }
 }
+// L2 policy of the state stream: evict-first by default (every state byte is read once).
+#ifndef C128_L2_POLICY
+#define C128_L2_POLICY 1
+#endif
 __device__ __forceinline__ uint64_t l2_evict_first_policy() {
   uint64_t pol;
+#if C128_L2_POLICY == 1
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+#else
+  asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(pol));
+#endif
   return pol;
 }
 // TMA bulk copy global -> shared; completion is counted in bytes on `bar`.

@@ -56,6 +56,8 @@ def lib() -> ctypes.CDLL:
             L.c128o_bf16.restype = ctypes.c_uint16
             L.c128o_e4m3.argtypes = [ctypes.c_float]
             L.c128o_e4m3.restype = ctypes.c_uint8
+            L.c128o_rsqrt.argtypes = [ctypes.c_float]
+            L.c128o_rsqrt.restype = ctypes.c_float
             L.c128o_ceil_log2.argtypes = [ctypes.c_float]
             L.c128o_ceil_log2.restype = ctypes.c_int
             L.c128o_mean_square_512.argtypes = [f32p]
@@ -97,6 +99,10 @@ def e4m3_code(x: float) -> int:
 
 def ceil_log2(x: float) -> int:
     return int(lib().c128o_ceil_log2(ctypes.c_float(x)))
+
+
+def rsqrt(x: float) -> np.float32:
+    return np.float32(lib().c128o_rsqrt(ctypes.c_float(x)))
 
 
 def bf16_bits_array(x: np.ndarray) -> np.ndarray:

@@ -17,7 +17,7 @@
  *   - positions < 0 are inactive (the pages' modulo would call p = -1 a window end);
  *   - softmax and weighted sum are evaluated in binary64 and rounded once to fp32 (comp32);
  *   - variance = RN32( exact(sum c^2) / 512 ), the sum taken exactly (big-integer accumulator);
- *   - rrms = RN32( 1.0 / sqrt((double)RN32(var + eps)) ) in IEEE binary64;
+ *   - rrms = the correctly rounded fp32 1/sqrt(RN32(var + eps)) (computed in binary64);
  *   - every other fp32 product / sum is one IEEE fp32 operation, left to right, no FMA;
  *   - fp32 -> bf16 and fp32 -> e4m3 round to nearest, ties to even; e4m3 saturates at 448
  *     and keeps the sign (so -0 and negative underflow give 0x80);
@@ -145,6 +145,12 @@ float c128o_mean_square_512(const float* c) {
 }
 
 /* ---------------------------------------------------------------------------------------- */
+/* rrms = RN32(1 / sqrt(v)), evaluated as IEEE binary64 sqrt and division rounded once to fp32. */
+/* For every positive finite fp32 v this is the correctly rounded reciprocal square root       */
+/* (checked exhaustively over all 2^31 - 2^23 - 1 such v by tests/rsqrt_exhaustive.c).         */
+float c128o_rsqrt(float v) { return (float)(1.0 / sqrt((double)v)); }
+
+/* ---------------------------------------------------------------------------------------- */
 /* RMSNorm -> quant -> RoPE on one compressed vector, producing the 576 token bytes and the   */
 /* 8 scale bytes of one k_cache slot.                                                          */
 void c128o_epilogue(const float* comp32, const float* rms_w, float eps, const float* cos_sin_row,
@@ -152,7 +158,7 @@ void c128o_epilogue(const float* comp32, const float* rms_w, float eps, const fl
     /* RMSNorm: variance = sum(c^2)/512, rrms = rsqrt(variance + eps), normed = c * rrms * w */
     float var32 = c128o_mean_square_512(comp32);
     float v = var32 + eps;
-    float rrms = (float)(1.0 / sqrt((double)v));
+    float rrms = c128o_rsqrt(v);
     float normed[HEAD];
     for (int c = 0; c < HEAD; ++c) {
         float t = comp32[c] * rrms;

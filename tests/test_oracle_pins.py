@@ -514,3 +514,40 @@ def test_golden_tiny_regression():
     oracle.forward(p, comp_out=comp)
     assert kc.tobytes().hex() == g["k_cache_hex"]
     assert comp.tobytes().hex() == g["comp32_hex"]
+
+
+# ------------------------------------------------------------------------------ rsqrt step
+def test_rsqrt_is_correctly_rounded_fraction():
+    """The oracle's rrms step against exact rational arithmetic: y is correctly rounded iff the
+    midpoints to its neighbours bracket 1/sqrt(v), i.e. md^2 v < 1 < mu^2 v."""
+    rng = np.random.default_rng(51)
+    u = rng.integers(1, 0x7F800000, size=20_000, dtype=np.uint64).astype(np.uint32)
+    vals = np.concatenate([u.view(np.float32), np.float32([1.0, 2.0, 0.5, 1e-6, 3.0, 1e-45, 3.4e38])])
+    for v in vals:
+        y = oracle.rsqrt(v)
+        up, dn = np.nextafter(y, np.float32(np.inf)), np.nextafter(y, np.float32(0))
+        fv, fy = Fraction(float(v)), Fraction(float(y))
+        mu, md = (fy + Fraction(float(up))) / 2, (fy + Fraction(float(dn))) / 2
+        assert md * md * fv < 1 < mu * mu * fv, float(v)
+
+
+def test_rsqrt_exhaustive_check_program():
+    """Compile tests/rsqrt_exhaustive.c and run it over every 509th positive fp32 pattern (all of
+    them when C128_EXHAUSTIVE=1: 2,139,095,039 values, about a minute on 8 cores)."""
+    import subprocess
+    import tempfile
+    src = os.path.join(os.path.dirname(__file__), "rsqrt_exhaustive.c")
+    exe = os.path.join(tempfile.mkdtemp(), "rsqrt_exhaustive")
+    subprocess.check_call([os.environ.get("CC", "cc"), "-O2", "-ffp-contract=off", "-o", exe, src, "-lm"])
+    full = os.environ.get("C128_EXHAUSTIVE") == "1"
+    step = 1 if full else 509
+    n = 8
+    bounds = [1 + i * ((0x7F800000 - 1) // n) for i in range(n)] + [0x7F800000]
+    procs = [subprocess.Popen([exe, str(bounds[i]), str(bounds[i + 1]), str(step)], stdout=subprocess.PIPE, text=True)
+             for i in range(n)]
+    total = 0
+    for pr in procs:
+        out, _ = pr.communicate()
+        assert pr.returncode == 0, out
+        total += int(out.split()[1])
+    assert total >= (0x7F800000 - 1) // step - n
