@@ -108,6 +108,69 @@ def check_against_oracle(problem, kc_gpu, comp_gpu, threads=8, tokens=None):
             if d2[a].any() or d2[b].any():
                 bad_windows += 1
                 assert not np.array_equal(comp_gpu[t].view(np.uint32), comp_ref[t].view(np.uint32))
+        _, max_deq, max_rope = slots_agree(problem, kc_gpu, kc_ref, rows_ref)
         out.update(e2e_bytes_differ=int(d2.sum()), e2e_windows_differ=bad_windows,
-                   fp8_codes_differ=int(sum(d2[slot_ranges(problem, t)[0]][:448].sum() for t in rows_ref)))
+                   fp8_codes_differ=int(sum(d2[slot_ranges(problem, t)[0]][:448].sum() for t in rows_ref)),
+                   max_dequant_diff=max_deq, max_rope_diff=max_rope)
     return out
+
+
+# --------------------------------------------------------------- byte-level agreement of two runs
+def _e4m3_table() -> np.ndarray:
+    """Value of every e4m3fn byte from the format definition (bias 7, 3 mantissa bits)."""
+    out = np.zeros(256)
+    for c in range(256):
+        E, m = (c >> 3) & 15, c & 7
+        v = (m / 8.0) * 2.0 ** -6 if E == 0 else (1 + m / 8.0) * 2.0 ** (E - 7)
+        out[c] = -v if c & 0x80 else v
+    out[0x7F] = out[0xFF] = np.nan
+    return out
+
+
+E4M3 = _e4m3_table()
+
+
+def _e4m3_step(y):
+    """Spacing of e4m3 codes around magnitude y (code space)."""
+    a = np.abs(y)
+    return np.where(a < 2.0 ** -6, 2.0 ** -9, 2.0 ** (np.floor(np.log2(np.maximum(a, 2.0 ** -6))) - 3))
+
+
+def slots_agree(problem, kc_a, kc_b, rows):
+    """Two runs of the op whose compressed vectors differ only by rounding: every byte outside
+    the stored slots is identical; inside them, scale bytes differ by at most 1 and every
+    dequantised nope value (e4m3 x 2^(scale-127)) by at most one quantisation step and every rope
+    value (bf16) by one bf16 step plus 1e-4 (the rotation can cancel). Returns (slots that differ, max dequant diff, max rope diff), the
+    quantities the pages report when they validate a kernel against another (PR #44230,
+    Validation)."""
+    fa, fb = kc_a.reshape(-1), kc_b.reshape(-1)
+    inside = np.zeros(fa.size, bool)
+    differ, max_deq, max_rope = 0, 0.0, 0.0
+    for t in rows:
+        tok, sc = slot_ranges(problem, t)
+        inside[tok] = True
+        inside[sc] = True
+        if np.array_equal(fa[tok], fb[tok]) and np.array_equal(fa[sc], fb[sc]):
+            continue
+        differ += 1
+        sa, sb = fa[sc].astype(int), fb[sc].astype(int)
+        assert sa[7] == sb[7] == 0 and np.all(np.abs(sa[:7] - sb[:7]) <= 1), (t, sa, sb)
+        ya = E4M3[fa[tok][:448]].reshape(7, 64)
+        yb = E4M3[fb[tok][:448]].reshape(7, 64)
+        pa = 2.0 ** (sa[:7] - 127.0)[:, None]
+        pb = 2.0 ** (sb[:7] - 127.0)[:, None]
+        va, vb = ya * pa, yb * pb
+        tol = np.maximum(_e4m3_step(ya) * pa, _e4m3_step(yb) * pb) * 1.001
+        d = np.abs(va - vb)
+        assert np.all(d <= tol), (t, float(d.max()))
+        max_deq = max(max_deq, float(d.max()))
+        ra = (fa[tok][448:].view(np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+        rb = (fb[tok][448:].view(np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+        dr = np.abs(ra - rb)
+        # one bf16 step of the output, plus an absolute 1e-4 for cancellation in e*C - o*S: the
+        # inputs are O(1) after RMSNorm and move by about 1e-5 relative when comp does
+        tol_r = np.maximum(np.abs(ra), np.abs(rb)) * 2.0 ** -7 + 1e-4
+        assert np.all(dr <= tol_r), (t, float(dr.max()))
+        max_rope = max(max_rope, float(dr.max()))
+    assert np.array_equal(fa[~inside], fb[~inside]), "bytes outside the stored slots differ"
+    return differ, max_deq, max_rope
