@@ -348,12 +348,12 @@ def traffic_per_launch(T: int):
 def sweep(args, dev):
     """µs per call vs token_num. Before every timed call a 512 MB buffer is written (L2 flush); the
     flush, the events and the call are enqueued back to back and synchronised once per size, so
-    host launch time hides behind the flush. Two columns: eager calls, and CUDA-graph replays of
-    the same call."""
+    host launch time hides behind the flush. Columns: eager calls, CUDA-graph replays of the same
+    call, and the pages' method (four input sets in rotation, back to back, no flush)."""
     import torch
     from deepseek_v4_sparse_c128_gb300 import binding
     flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
-    eager, graph = {}, {}
+    eager, graph, rot4 = {}, {}, {}
     for T in inputs.SWEEP_TOKENS:
         p = inputs.make_problem("sweep", tokens=T, state_device=str(dev))
         to = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
@@ -372,6 +372,26 @@ def sweep(args, dev):
             with torch.cuda.graph(g, stream=s):
                 call()
             n = 50 if T < 4096 else 20
+            # the pages' method (PR #44230, Performance: bench_inputs=4): four input sets used in
+            # rotation, no flush in between, so small sizes partly hit L2
+            sets = [call]
+            for k in range(1, 4):
+                dk = dict(d)
+                dk["k_cache"] = d["k_cache"].clone()
+                st_k = inputs.draw_state(1000 + k, p.state.shape[0], str(dev))
+                sets.append(binding.PreparedCall(dk["token_to_req"], dk["positions"], dk["slot_mapping"],
+                                                 dk["block_table"], st_k, dk["rms_w"], p.eps, dk["cos_sin"],
+                                                 dk["k_cache"], dk["kv_slot_mapping"], p.kv_block_size, stream=s))
+            for c in sets:
+                c()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(s)
+            for i in range(4 * n):
+                sets[i % 4]()
+            b.record(s)
+            s.synchronize()
+            rot4[str(T)] = round(a.elapsed_time(b) * 1e3 / (4 * n), 3)
+            del sets
             for mode, fn in (("eager", call), ("graph", g.replay)):
                 evs = []
                 for _ in range(n):
@@ -386,7 +406,7 @@ def sweep(args, dev):
                 (eager if mode == "eager" else graph)[str(T)] = round(us, 3)
             assert binding.device_errors(s, clear=True) == 0
         del d, p, g, call
-    return {"eager": eager, "graph": graph}
+    return {"eager": eager, "graph": graph, "rotate4_no_flush": rot4}
 
 
 # --------------------------------------------------------------------------- reference arm
