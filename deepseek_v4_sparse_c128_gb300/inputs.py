@@ -39,6 +39,8 @@ ROPE = 64
 TOKEN_BYTES = 584     # 448 fp8 + 64 bf16 (= 576 B) + 8 scale bytes per token
 
 SWEEP_TOKENS = (1, 2, 4, 8, 16, 32, 64, 128, 256, 512, 1024, 2048, 4096, 8192, 16374)
+# slot bytes (token data + scales) of each cache format
+SLOT_BYTES = {0: 576 + 8, 1: 128 + 4, 2: 64 + 4}
 CONFIG_SEEDS = {"tiny": 0, "decode": 1, "mixed": 2, "varlen": 3, "sweep": 4, "varlen16k": 5}
 
 
@@ -55,9 +57,15 @@ class Problem:
     rms_w: np.ndarray             # float32 [512]
     eps: float
     cos_sin: np.ndarray           # float32 [MP, 64]
-    k_cache: np.ndarray           # uint8 [NKB, bs, 584]
+    k_cache: np.ndarray           # uint8 [NKB, bs, slot bytes]
     kv_slot_mapping: np.ndarray   # int64 [T]
     kv_block_size: int
+    # configuration (defaults: the C128 sparse-attention compressor)
+    head: int = 512               # 512 (sparse attention) or 128 (indexer)
+    ratio: int = 128              # compress ratio
+    overlap: int = 0              # 1: windows of 2*ratio rows, the newer half at +head
+    state_width: int = 512        # kv columns of a state row; as many score columns follow
+    fmt: int = 0                  # cache format: 0 sparse FP8 + bf16 rope, 1 indexer FP8, 2 indexer MXFP4
 
     @property
     def num_tokens(self) -> int:
@@ -251,6 +259,85 @@ def make_problem(name: str, seed: Optional[int] = None, tokens: Optional[int] = 
         T = tokens if tokens is not None else int(name[5:] or 16374)
         return _sweep(seed, T, state_device)
     raise ValueError(f"unknown workload {name!r}")
+
+
+def draw_state_rows(seed: int, num_blocks: int, block: int, state_width: int, device: str = "cpu"):
+    """State cache [num_blocks, block, 2*state_width]: kv ~ N(0,1) then score ~ N(0,2) in every row."""
+    if device == "none":
+        return None
+    if device == "cpu":
+        rng = np.random.default_rng([seed, 0x5EED, state_width])
+        st = rng.standard_normal((num_blocks, block, 2 * state_width), dtype=np.float32)
+        st[..., state_width:] *= np.float32(2.0)
+        return st
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed) * 1000003 + 29)
+    st = torch.randn((num_blocks, block, 2 * state_width), generator=g, device=device, dtype=torch.float32)
+    st[..., state_width:] *= 2.0
+    return st
+
+
+def prefill_problem(name: str, seed: int, num_reqs: int, min_len: int, max_len: int, head: int, ratio: int,
+                    overlap: int, fmt: int, state_block: int = 8, kv_block_size: int = 64,
+                    state_device: str = "cpu", decode_tail: int = 0) -> Problem:
+    """Requests with every position 0..len-1 present (window ends active: every `ratio`-th token),
+    request-major, blocks from a shuffled pool; optionally `decode_tail` extra one-token requests
+    at window ends. State width is head * (1 + overlap)."""
+    rng = np.random.default_rng([seed, ratio, head, fmt])
+    sw = head * (1 + overlap)
+    lens = rng.integers(min_len, max_len + 1, size=num_reqs).astype(np.int64)
+    if decode_tail:
+        k = rng.integers(1, 65, size=decode_tail) if ratio >= 128 else rng.integers(8, 512, size=decode_tail)
+        lens = np.concatenate([lens, ratio * k])
+    R = lens.shape[0]
+    nblk = (lens + state_block - 1) // state_block
+    NB, MB = int(nblk.sum()), int(nblk.max())
+    pool = rng.permutation(NB)
+    bt = rng.integers(0, NB, size=(R, MB)).astype(np.int32)
+    off = 0
+    for r in range(R):
+        bt[r, :nblk[r]] = pool[off:off + nblk[r]]
+        off += nblk[r]
+    if decode_tail:   # the one-token requests carry only their last position
+        req = np.concatenate([np.repeat(np.arange(num_reqs, dtype=np.int32), lens[:num_reqs]),
+                              np.arange(num_reqs, R, dtype=np.int32)])
+        pos = np.concatenate([np.concatenate([np.arange(n, dtype=np.int64) for n in lens[:num_reqs]]),
+                              lens[num_reqs:] - 1])
+    else:
+        req = np.repeat(np.arange(R, dtype=np.int32), lens)
+        pos = np.concatenate([np.arange(n, dtype=np.int64) for n in lens])
+    slot = _state_slot_blocks(bt, req, pos, state_block)
+    active = (pos + 1) % ratio == 0
+    A = int(active.sum())
+    NKB = max(1, -(-A // kv_block_size))
+    kv_slot = np.full(pos.shape[0], -1, dtype=np.int64)
+    kv_slot[np.nonzero(active)[0]] = rng.permutation(NKB * kv_block_size)[:A]
+    max_pos = int(pos.max()) + 1
+    return Problem(name, req, pos, slot, bt, draw_state_rows(seed, NB, state_block, sw, state_device),
+                   _rms_w(rng)[:head].copy(), 1e-6, _cos_sin_cache(max_pos),
+                   rng.integers(0, 256, size=(NKB, kv_block_size, SLOT_BYTES[fmt]), dtype=np.uint8), kv_slot,
+                   kv_block_size, head=head, ratio=ratio, overlap=overlap, state_width=sw, fmt=fmt)
+
+
+def _state_slot_blocks(block_table, req, pos, state_block):
+    blk = block_table[req, pos // state_block].astype(np.int64)
+    return blk * state_block + pos % state_block
+
+
+def make_next_problem(name: str, state_device: str = "cpu", scale: int = 1) -> Problem:
+    """Workloads for the other configurations: C4 sparse attention (head 512, ratio 4, overlap),
+    the indexer (head 128) with FP8 or MXFP4 caches at ratio 4 with overlap and at ratio 128."""
+    spec = {
+        "c4_sparse": (512, 4, 1, 0), "idx_c4_fp8": (128, 4, 1, 1), "idx_c4_mxfp4": (128, 4, 1, 2),
+        "idx_c128_fp8": (128, 128, 0, 1), "idx_c128_mxfp4": (128, 128, 0, 2),
+    }[name]
+    head, ratio, overlap, fmt = spec
+    if ratio == 4:
+        return prefill_problem(name, 6, 8 * scale, 5, 1024, head, ratio, overlap, fmt, state_device=state_device,
+                               decode_tail=16 * scale)
+    return prefill_problem(name, 7, 4 * scale, 128, 8192, head, ratio, overlap, fmt, state_device=state_device,
+                           decode_tail=64 * scale)
 
 
 def random_problem(seed: int, num_tokens: int, num_reqs: int, max_blocks: int, num_blocks: int,

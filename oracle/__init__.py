@@ -30,6 +30,14 @@ _lib = None
 HEAD = 512
 TOKEN_STRIDE = 576
 SCALE_DIM = 8
+# token / scale bytes per k_cache slot of each cache format (0: sparse attention, 1: indexer FP8,
+# 2: indexer MXFP4)
+FORMAT_BYTES = {0: (576, 8), 1: (128, 4), 2: (64, 4)}
+
+
+class Cfg(ctypes.Structure):
+    _fields_ = [("head", ctypes.c_int32), ("rope", ctypes.c_int32), ("ratio", ctypes.c_int32),
+                ("overlap", ctypes.c_int32), ("state_width", ctypes.c_int32), ("format", ctypes.c_int32)]
 
 
 def build(force: bool = False) -> str:
@@ -70,6 +78,17 @@ def lib() -> ctypes.CDLL:
                                         f32p, ctypes.c_float, f32p, i64, i64, u8p, i64, i64, i64, i64p,
                                         f32p, i64p, i64]
             L.c128o_forward.restype = ctypes.c_int
+            L.c128o_e2m1.argtypes = [ctypes.c_float]
+            L.c128o_e2m1.restype = ctypes.c_uint8
+            L.c128o_mean_square_128.argtypes = [f32p]
+            L.c128o_mean_square_128.restype = ctypes.c_float
+            for name in ("c128o_epilogue_indexer_fp8", "c128o_epilogue_indexer_mxfp4"):
+                getattr(L, name).argtypes = [f32p, f32p, ctypes.c_float, f32p, u8p, u8p]
+                getattr(L, name).restype = None
+            L.c128o_forward_ex.argtypes = [ctypes.POINTER(Cfg), i64, i32p, i64p, i64p, i32p, i64, i64, i64, f32p,
+                                           i64, i64, i64, i64, f32p, ctypes.c_float, f32p, i64, i64, u8p, i64, i64,
+                                           i64, i64p, f32p, i64p, i64]
+            L.c128o_forward_ex.restype = ctypes.c_int
             L.c128o_bf16_n.argtypes = [f32p, ctypes.POINTER(ctypes.c_uint16), i64]
             L.c128o_bf16_n.restype = None
             L.c128o_e4m3_n.argtypes = [f32p, u8p, i64]
@@ -117,6 +136,28 @@ def e4m3_codes(x: np.ndarray) -> np.ndarray:
     out = np.zeros(x.shape, np.uint8)
     lib().c128o_e4m3_n(_ptr(x, ctypes.c_float), _ptr(out, ctypes.c_uint8), x.size)
     return out
+
+
+def e2m1_code(x: float) -> int:
+    return int(lib().c128o_e2m1(ctypes.c_float(x)))
+
+
+def mean_square_128(c: np.ndarray) -> np.float32:
+    c = _c(c, np.float32)
+    assert c.shape == (128,)
+    return np.float32(lib().c128o_mean_square_128(_ptr(c, ctypes.c_float)))
+
+
+def epilogue_indexer(fmt: int, comp32: np.ndarray, rms_w: np.ndarray, eps: float, cos_sin_row: np.ndarray):
+    """Indexer epilogue of one 128-wide compressed vector: fmt 1 -> (128 e4m3 bytes, 4 bytes of
+    fp32 scale), fmt 2 -> (64 bytes of E2M1 pairs, 4 UE8M0 bytes)."""
+    comp32, rms_w, cs = _c(comp32, np.float32), _c(rms_w, np.float32), _c(cos_sin_row, np.float32)
+    nt, ns = FORMAT_BYTES[fmt]
+    tok, sc = np.zeros(nt, np.uint8), np.zeros(ns, np.uint8)
+    fn = lib().c128o_epilogue_indexer_fp8 if fmt == 1 else lib().c128o_epilogue_indexer_mxfp4
+    fn(_ptr(comp32, ctypes.c_float), _ptr(rms_w, ctypes.c_float), ctypes.c_float(eps), _ptr(cs, ctypes.c_float),
+       _ptr(tok, ctypes.c_uint8), _ptr(sc, ctypes.c_uint8))
+    return tok, sc
 
 
 def mean_square_512(c: np.ndarray) -> np.float32:
@@ -194,6 +235,54 @@ def forward(problem, k_cache: Optional[np.ndarray] = None, tokens: Optional[Sequ
             err = 0
             for e in ex.map(run, chunks):
                 err |= e
+    return err
+
+
+def problem_cfg(problem) -> Cfg:
+    return Cfg(getattr(problem, "head", 512), 64, getattr(problem, "ratio", 128), getattr(problem, "overlap", 0),
+               getattr(problem, "state_width", 512), getattr(problem, "fmt", 0))
+
+
+def forward_ex(problem, k_cache: Optional[np.ndarray] = None, tokens: Optional[Sequence[int]] = None,
+               comp_out: Optional[np.ndarray] = None, threads: int = 1) -> int:
+    """The op for any configuration (head, compress ratio, overlap, state width, cache format) the
+    problem carries; same conventions as forward(). comp_out is [T, head]."""
+    L = lib()
+    cfg = problem_cfg(problem)
+    state = problem.state
+    assert isinstance(state, np.ndarray) and state.dtype == np.float32 and state.flags.c_contiguous
+    ttr, pos = _c(problem.token_to_req, np.int32), _c(problem.positions, np.int64)
+    slot, bt = _c(problem.slot_mapping, np.int64), _c(problem.block_table, np.int32)
+    kvs, rms_w = _c(problem.kv_slot_mapping, np.int64), _c(problem.rms_w, np.float32)
+    cs = _c(problem.cos_sin, np.float32)
+    if k_cache is None:
+        k_cache = problem.k_cache.copy()
+    assert k_cache.dtype == np.uint8 and k_cache.flags.c_contiguous
+    T = pos.shape[0]
+    if comp_out is not None:
+        assert comp_out.dtype == np.float32 and comp_out.shape == (T, cfg.head) and comp_out.flags.c_contiguous
+    all_tok = np.arange(T, dtype=np.int64) if tokens is None else np.asarray(tokens, dtype=np.int64)
+    chunks = np.array_split(all_tok, max(1, threads)) if threads > 1 else [all_tok]
+    NB, BS, RW = state.shape
+
+    def run(sub):
+        sub = np.ascontiguousarray(sub, dtype=np.int64)
+        return L.c128o_forward_ex(
+            ctypes.byref(cfg), T, _ptr(ttr, ctypes.c_int32), _ptr(pos, ctypes.c_int64), _ptr(slot, ctypes.c_int64),
+            _ptr(bt, ctypes.c_int32), bt.shape[0], bt.shape[1], bt.shape[1], _ptr(state, ctypes.c_float), NB, BS,
+            BS * RW, RW, _ptr(rms_w, ctypes.c_float), ctypes.c_float(problem.eps), _ptr(cs, ctypes.c_float),
+            cs.shape[0], cs.shape[1], _ptr(k_cache, ctypes.c_uint8), k_cache.shape[0], problem.kv_block_size,
+            k_cache.shape[1] * k_cache.shape[2], _ptr(kvs, ctypes.c_int64),
+            _ptr(comp_out, ctypes.c_float) if comp_out is not None else None, _ptr(sub, ctypes.c_int64), sub.shape[0])
+
+    if len(chunks) == 1:
+        err = run(chunks[0])
+    else:
+        with ThreadPoolExecutor(len(chunks)) as ex:
+            err = 0
+            for e in ex.map(run, chunks):
+                err |= e
+    assert err >= 0, "unsupported configuration"
     return err
 
 

@@ -97,10 +97,11 @@ int c128o_ceil_log2(float r) {
 /* integer multiple of 2^-344 (smallest fp32 magnitude 2^-149 has e = -148). A 640-bit         */
 /* accumulator of 32-bit limbs holds every term and the 512-term sum without loss.              */
 #define NLIMB 20
-float c128o_mean_square_512(const float* c) {
+/* RN32( (sum_i c_i^2) / 2^log2n ) over n = 2^log2n <= 512 values, the sum taken exactly. */
+static float exact_mean_square(const float* c, int n, int log2n) {
     uint32_t acc[NLIMB];
     memset(acc, 0, sizeof acc);
-    for (int i = 0; i < HEAD; ++i) {
+    for (int i = 0; i < n; ++i) {
         float x = fabsf(c[i]);
         if (x == 0.0f) continue;
         if (!isfinite(x)) return isnan(x) ? NAN : INFINITY; /* not reached by finite inputs */
@@ -124,15 +125,15 @@ float c128o_mean_square_512(const float* c) {
             carry = s >> 32;
         }
     }
-    /* value = acc * 2^-344 / 512 = acc * 2^-353; round to fp32 (normal or subnormal), RNE. */
+    /* value = acc * 2^-344 / 2^log2n; round to fp32 (normal or subnormal), RNE. */
     int msb = -1;
     for (int j = NLIMB - 1; j >= 0 && msb < 0; --j)
         if (acc[j]) for (int b = 31; b >= 0; --b) if (acc[j] >> b & 1u) { msb = 32 * j + b; break; }
     if (msb < 0) return 0.0f;
-    const int k = -353;
+    const int k = -344 - log2n;
     int lsb = msb - 23;
     if (lsb < -149 - k) lsb = -149 - k;               /* subnormal results keep fewer bits */
-    /* lsb >= 204 here, so there is always a round bit below it */
+    /* lsb >= 195 + log2n > 0 here, so there is always a round bit below it */
     uint64_t q = 0;
     int round_up = 0;
     for (int b = msb; b >= lsb; --b) q = (q << 1) | (acc[b / 32] >> (b % 32) & 1u);
@@ -143,6 +144,8 @@ float c128o_mean_square_512(const float* c) {
     q += (uint64_t)round_up;
     return (float)ldexp((double)q, lsb + k);         /* exact; >= 2^128 becomes +inf */
 }
+float c128o_mean_square_512(const float* c) { return exact_mean_square(c, HEAD, 9); }
+float c128o_mean_square_128(const float* c) { return exact_mean_square(c, 128, 7); }
 
 /* ---------------------------------------------------------------------------------------- */
 /* rrms = RN32(1 / sqrt(v)), evaluated as IEEE binary64 sqrt and division rounded once to fp32. */
@@ -287,4 +290,204 @@ void c128o_bf16_n(const float* x, uint16_t* out, int64_t n) {
 }
 void c128o_e4m3_n(const float* x, uint8_t* out, int64_t n) {
     for (int64_t i = 0; i < n; ++i) out[i] = c128o_e4m3(x[i]);
+}
+
+
+/* ========================================================================================== */
+/* The other configurations of the fused kernels on the API page:                             */
+/*   format 0  _fused_kv_compress_norm_rope_insert_sparse_attn  (head 512: nope FP8 + rope bf16) */
+/*   format 1  _fused_kv_compress_norm_rope_insert_indexer_attn (head 128: RoPE, then one FP8    */
+/*             block with an fp32 power-of-two scale)                                           */
+/*   format 2  _fused_kv_compress_norm_rope_insert_indexer_mxfp4_attn (head 128: RoPE, bf16     */
+/*             round, MXFP4 E2M1 pairs with one UE8M0 byte per 32 values)                       */
+/* with any compress ratio, with or without overlap ("Gather state cache entries": 2*ratio rows */
+/* when overlapping; the newer `ratio` rows read kv and score at +head; rows at negative        */
+/* positions are left out of the softmax). A state row is kv[state_width] then score[state_width]. */
+typedef struct c128o_cfg {
+    int32_t head;         /* 512 (format 0) or 128 (formats 1, 2) */
+    int32_t rope;         /* 64 */
+    int32_t ratio;        /* compress ratio (window end: (p+1) % ratio == 0) */
+    int32_t overlap;      /* 0 or 1 */
+    int32_t state_width;  /* kv columns of a state row; as many score columns follow */
+    int32_t format;       /* 0, 1, 2 as above */
+} c128o_cfg;
+
+#define IDX_HEAD 128
+#define IDX_TOKEN_FP8 128    /* indexer FP8: 128 e4m3 bytes per token, then one fp32 scale */
+#define IDX_TOKEN_FP4 64     /* indexer MXFP4: 64 bytes of E2M1 pairs, then 4 UE8M0 bytes */
+#define IDX_SCALE_DIM 4
+
+/* E2M1 (OCP MXFP4 element): sign, 2 exponent bits (bias 1), 1 mantissa bit; magnitudes
+ * 0, 0.5, 1, 1.5, 2, 3, 4, 6. Nearest by exhaustive search, ties to the even code, values beyond
+ * 6 saturate, the sign bit of x is kept. (The page's _fp32x2_to_fp4x2 body is not printed; this
+ * round-to-nearest-even, saturating reading is the one the design notes list.) */
+uint8_t c128o_e2m1(float x) {
+    static const double mag[8] = {0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0};
+    double a = fabs((double)x);
+    int best = 0;
+    double bestd = a;
+    for (int c = 1; c < 8; ++c) {
+        double d = fabs(mag[c] - a);
+        if (d < bestd || (d == bestd && (c & 1) == 0 && (best & 1) == 1)) { best = c; bestd = d; }
+    }
+    return (uint8_t)(best | ((f2u(x) >> 31) ? 0x8 : 0));
+}
+
+/* Softmax-weighted sum of one window for `head` columns: rows[i] == NULL marks a masked row;
+ * kv of row i at rows[i][koff[i] + c], its score at rows[i][soff[i] + c]. binary64, one rounding. */
+static void compress_window_ex(int nrows, const float* const* rows, const int* koff, const int* soff, int head,
+                               float* comp32) {
+    for (int c = 0; c < head; ++c) {
+        double m = -INFINITY;
+        for (int i = 0; i < nrows; ++i) {
+            if (!rows[i]) continue;
+            double s = rows[i][soff[i] + c];
+            if (s > m) m = s;
+        }
+        double Z = 0.0, acc = 0.0;
+        double w[256];
+        for (int i = 0; i < nrows; ++i) {
+            w[i] = rows[i] ? exp((double)rows[i][soff[i] + c] - m) : 0.0;
+            Z += w[i];
+        }
+        for (int i = 0; i < nrows; ++i)
+            if (rows[i]) acc += (w[i] / Z) * (double)rows[i][koff[i] + c];
+        comp32[c] = (float)acc;
+    }
+}
+
+/* RMSNorm over 128 columns then GPT-J RoPE of every pair, the 32 nope pairs with cos 1, sin 0
+ * exactly as the page writes it (its masked loads give those values), the 32 rope pairs with
+ * cos/sin of the window row. Output: the rotated fp32 pairs, even then odd. */
+static void indexer_norm_rope(const float* comp32, const float* rms_w, float eps, const float* cs_row,
+                              float* even, float* odd) {
+    float var32 = c128o_mean_square_128(comp32);
+    float rrms = c128o_rsqrt(var32 + eps);
+    float normed[IDX_HEAD];
+    for (int c = 0; c < IDX_HEAD; ++c) {
+        float t = comp32[c] * rrms;
+        normed[c] = t * rms_w[c];
+    }
+    const int nope_pairs = (IDX_HEAD - 64) / 2;
+    for (int j = 0; j < IDX_HEAD / 2; ++j) {
+        float ev = normed[2 * j], od = normed[2 * j + 1];
+        float C = 1.0f, S = 0.0f;
+        if (j >= nope_pairs) { C = cs_row[j - nope_pairs]; S = cs_row[32 + j - nope_pairs]; }
+        float ec = ev * C, os = od * S, oc = od * C, es = ev * S;
+        even[j] = ec - os;
+        odd[j] = oc + es;
+    }
+}
+
+/* format 1: bf16 round, one absmax over 128 (floor 1e-4), e = ceil(log2(absmax * RN32(1/448))),
+ * 128 e4m3 codes of clamp(x * 2^-e, +-448), fp32 scale 2^e stored little-endian. */
+void c128o_epilogue_indexer_fp8(const float* comp32, const float* rms_w, float eps, const float* cs_row,
+                                uint8_t* token_bytes, uint8_t* scale_bytes) {
+    float even[IDX_HEAD / 2], odd[IDX_HEAD / 2], x[IDX_HEAD];
+    indexer_norm_rope(comp32, rms_w, eps, cs_row, even, odd);
+    float amax = 0.0f;
+    for (int j = 0; j < IDX_HEAD / 2; ++j) {
+        x[2 * j] = bf16_value(even[j]);
+        x[2 * j + 1] = bf16_value(odd[j]);
+    }
+    for (int c = 0; c < IDX_HEAD; ++c) if (fabsf(x[c]) > amax) amax = fabsf(x[c]);
+    if (amax < (float)1e-4) amax = (float)1e-4;
+    float raw = amax * (float)(1.0 / 448.0);
+    int e = c128o_ceil_log2(raw);
+    float inv_scale = (float)ldexp(1.0, -e);
+    for (int c = 0; c < IDX_HEAD; ++c) {
+        float y = x[c] * inv_scale;
+        if (y > FP8_MAX) y = FP8_MAX;
+        if (y < -FP8_MAX) y = -FP8_MAX;
+        token_bytes[c] = c128o_e4m3(y);
+    }
+    float scale = (float)ldexp(1.0, e);
+    uint32_t u = f2u(scale);
+    for (int b = 0; b < 4; ++b) scale_bytes[b] = (uint8_t)(u >> (8 * b));
+}
+
+/* format 2: bf16 round of the rotated pairs; per 32 values (16 pairs) amax (floor 6*2^-126),
+ * e = clamp(ceil(log2(amax * RN32(1/6))), -127, 127), E2M1 codes of x * 2^-e, byte j of the block =
+ * even code in the low nibble, odd code in the high nibble; UE8M0 byte e + 127. */
+void c128o_epilogue_indexer_mxfp4(const float* comp32, const float* rms_w, float eps, const float* cs_row,
+                                  uint8_t* token_bytes, uint8_t* scale_bytes) {
+    float even[IDX_HEAD / 2], odd[IDX_HEAD / 2];
+    indexer_norm_rope(comp32, rms_w, eps, cs_row, even, odd);
+    for (int j = 0; j < IDX_HEAD / 2; ++j) { even[j] = bf16_value(even[j]); odd[j] = bf16_value(odd[j]); }
+    const float floor_amax = (float)(6.0 * ldexp(1.0, -126));
+    const float inv6 = (float)(1.0 / 6.0);
+    for (int b = 0; b < IDX_HEAD / 32; ++b) {
+        float amax = 0.0f;
+        for (int j = 16 * b; j < 16 * b + 16; ++j) {
+            if (fabsf(even[j]) > amax) amax = fabsf(even[j]);
+            if (fabsf(odd[j]) > amax) amax = fabsf(odd[j]);
+        }
+        if (amax < floor_amax) amax = floor_amax;
+        int e = c128o_ceil_log2(amax * inv6);
+        if (e < -127) e = -127;
+        if (e > 127) e = 127;
+        float inv_scale = (float)ldexp(1.0, -e);
+        for (int j = 16 * b; j < 16 * b + 16; ++j)
+            token_bytes[j] = (uint8_t)(c128o_e2m1(even[j] * inv_scale) | (c128o_e2m1(odd[j] * inv_scale) << 4));
+        scale_bytes[b] = (uint8_t)(e + 127);
+    }
+}
+
+/* The op for any configuration above (same index arguments as c128o_forward; state rows of
+ * st_s1 >= 2 * state_width floats, blocks of `state_block` rows; comp_out is [T, head]). */
+int c128o_forward_ex(const c128o_cfg* cfg, int64_t num_tokens, const int32_t* token_to_req,
+                     const int64_t* positions, const int64_t* slot_mapping, const int32_t* block_table,
+                     int64_t num_reqs, int64_t bt_cols, int64_t bt_row_stride, const float* state,
+                     int64_t num_blocks, int64_t state_block, int64_t st_s0, int64_t st_s1,
+                     const float* rms_w, float eps, const float* cos_sin, int64_t max_pos, int64_t cs_stride,
+                     uint8_t* k_cache, int64_t num_kv_blocks, int64_t kv_block_size, int64_t kc_block_stride,
+                     const int64_t* kv_slot_mapping, float* comp_out, const int64_t* token_subset,
+                     int64_t n_subset) {
+    const int head = cfg->head, ratio = cfg->ratio, nrows = (1 + (cfg->overlap ? 1 : 0)) * ratio;
+    if (nrows > 256 || (cfg->format == 0 && head != HEAD) || (cfg->format != 0 && head != IDX_HEAD)) return -1;
+    const int64_t tok_bytes = cfg->format == 0 ? TOKEN_STRIDE : cfg->format == 1 ? IDX_TOKEN_FP8 : IDX_TOKEN_FP4;
+    const int64_t sc_bytes = cfg->format == 0 ? SCALE_DIM : IDX_SCALE_DIM;
+    int err = 0;
+    int64_t n = token_subset ? n_subset : num_tokens;
+    for (int64_t ii = 0; ii < n; ++ii) {
+        int64_t t = token_subset ? token_subset[ii] : ii;
+        if (t < 0 || t >= num_tokens) continue;
+        int64_t slot = slot_mapping[t], p = positions[t], kvs = kv_slot_mapping[t];
+        if (slot < 0 || p < 0 || (p + 1) % ratio != 0 || kvs < 0) continue;
+        int64_t r = token_to_req[t];
+        int terr = 0;
+        if (r < 0 || r >= num_reqs) terr |= ORC_BAD_REQ;
+        if (p / state_block >= bt_cols) terr |= ORC_BAD_BT_COL;
+        int64_t cp = (p / ratio) * ratio;
+        if (cp >= max_pos) terr |= ORC_BAD_COS_ROW;
+        if (kvs >= num_kv_blocks * kv_block_size) terr |= ORC_BAD_KV_SLOT;
+        const float* rows[256];
+        int koff[256], soff[256];
+        if (!(terr & (ORC_BAD_REQ | ORC_BAD_BT_COL))) {
+            int64_t start = p - nrows + 1;
+            for (int i = 0; i < nrows; ++i) {
+                int64_t q = start + i;
+                int ho = i >= ratio ? head : 0;
+                koff[i] = ho;
+                soff[i] = cfg->state_width + ho;
+                if (q < 0) { rows[i] = NULL; continue; }
+                int64_t b = block_table[r * bt_row_stride + q / state_block];
+                if (b < 0 || b >= num_blocks) { terr |= ORC_BAD_BLOCK; break; }
+                rows[i] = state + b * st_s0 + (q % state_block) * st_s1;
+            }
+        }
+        if (terr) { err |= terr; continue; }
+        float comp32[HEAD];
+        compress_window_ex(nrows, rows, koff, soff, head, comp32);
+        if (comp_out) memcpy(comp_out + t * head, comp32, sizeof(float) * head);
+        int64_t blk = kvs / kv_block_size, off = kvs % kv_block_size;
+        uint8_t* base = k_cache + blk * kc_block_stride;
+        uint8_t* tok = base + off * tok_bytes;
+        uint8_t* sc = base + kv_block_size * tok_bytes + off * sc_bytes;
+        const float* cs_row = cos_sin + cp * cs_stride;
+        if (cfg->format == 0) c128o_epilogue(comp32, rms_w, eps, cs_row, tok, sc);
+        else if (cfg->format == 1) c128o_epilogue_indexer_fp8(comp32, rms_w, eps, cs_row, tok, sc);
+        else c128o_epilogue_indexer_mxfp4(comp32, rms_w, eps, cs_row, tok, sc);
+    }
+    return err;
 }

@@ -551,3 +551,144 @@ def test_rsqrt_exhaustive_check_program():
         assert pr.returncode == 0, out
         total += int(out.split()[1])
     assert total >= (0x7F800000 - 1) // step - n
+
+
+# ------------------------------------------------- other configurations of the fused kernels
+E2M1_MAG = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+
+
+def test_e2m1_encoder_definition():
+    """E2M1: every code round-trips; ties go to the even code; beyond 6 saturates; sign kept."""
+    for c in range(16):
+        v = E2M1_MAG[c & 7] * (-1 if c & 8 else 1)
+        if c == 8:
+            continue
+        assert oracle.e2m1_code(v) == c, c
+    ties = {0.25: 0, 0.75: 2, 1.25: 2, 1.75: 4, 2.5: 4, 3.5: 6, 5.0: 6}
+    for v, c in ties.items():
+        assert oracle.e2m1_code(v) == c and oracle.e2m1_code(-v) == c | 8, v
+    assert oracle.e2m1_code(0.26) == 1 and oracle.e2m1_code(5.01) == 7
+    assert oracle.e2m1_code(7.0) == 7 and oracle.e2m1_code(1e9) == 7 and oracle.e2m1_code(-0.0) == 8
+    assert oracle.e2m1_code(-1e-30) == 8
+
+
+def test_mean_square_128_is_exact():
+    rng = np.random.default_rng(61)
+    for scale in (1.0, 1e-20, 1e18):
+        c = (rng.standard_normal(128) * scale).astype(np.float32)
+        want = rn32_of_fraction(sum((Fraction(float(v)) ** 2 for v in c), Fraction(0)) / 128)
+        assert oracle.mean_square_128(c).view(np.uint32) == want.view(np.uint32)
+
+
+def _pow2_signs(rng, n, mags):
+    return (rng.choice(mags, n) * rng.choice([-1.0, 1.0], n)).astype(np.float32)
+
+
+def test_indexer_fp8_epilogue_closed_form():
+    """Head 128: RMSNorm (var 1, eps 0), RoPE of the last 32 pairs only (cos at [j], sin at
+    [32+j]) BEFORE the quant, one absmax over all 128 values, fp32 scale 2^e stored LE."""
+    rng = np.random.default_rng(62)
+    for it in range(30):
+        comp = rng.choice([-1.0, 1.0], 128).astype(np.float32)        # mean square exactly 1
+        w = (rng.choice([1.0, 1.5, 1.25, 1.75], 128) * 2.0 ** rng.integers(-6, 3, 128)).astype(np.float32)
+        C, S = float(rng.choice([1.0, 0.0, -1.0, 0.5])), float(rng.choice([0.0, 1.0, -0.5]))
+        cs = np.concatenate([np.full(32, C, np.float32), np.full(32, S, np.float32)])
+        tok, sc = oracle.epilogue_indexer(1, comp, w, 0.0, cs)
+        normed = comp.astype(np.float64) * w
+        ev, od = normed[0::2].copy(), normed[1::2].copy()
+        ne, no = ev.copy(), od.copy()
+        ne[32:], no[32:] = ev[32:] * C - od[32:] * S, od[32:] * C + ev[32:] * S
+        x = np.empty(128)
+        x[0::2], x[1::2] = ne, no
+        assert np.array_equal(x.astype(np.float32).astype(np.float64), x)    # exact so far
+        x = bf16_to_f32(oracle.bf16_bits_array(x.astype(np.float32))).astype(np.float64)
+        amax = max(float(np.abs(x).max()), float(np.float32(1e-4)))
+        raw = Fraction(float(rn32_of_fraction(Fraction(amax) * Fraction(float(np.float32(1 / 448))))))
+        e = math.ceil(math.log2(float(raw)))
+        if Fraction(2) ** (e - 1) >= raw:
+            e -= 1
+        assert list(tok) == [_hand_code(float(np.clip(v * 2.0 ** -e, -448, 448))) for v in x]
+        assert sc.view(np.float32)[0] == np.float32(2.0 ** e)
+
+
+def test_indexer_mxfp4_epilogue_closed_form():
+    """MXFP4: per 32 values amax -> e = ceil(log2(amax/6)), E2M1 codes of x*2^-e, byte j = even
+    code | odd code << 4, UE8M0 byte e + 127; values chosen E2M1-exact at each block's scale."""
+    rng = np.random.default_rng(63)
+    inv6 = Fraction(float(np.float32(1 / 6)))
+    for it in range(30):
+        comp = rng.choice([-1.0, 1.0], 128).astype(np.float32)
+        w = np.zeros(128, np.float32)
+        ks = rng.integers(-10, 6, 4)
+        for b in range(4):
+            m = rng.choice([0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0], 32)
+            m[rng.integers(0, 32)] = 6.0                                  # block max exactly 6 * 2^k
+            w[32 * b:32 * b + 32] = (m * 2.0 ** ks[b]).astype(np.float32)
+        cs = np.concatenate([np.ones(32, np.float32), np.zeros(32, np.float32)])  # rope = identity
+        tok, sc = oracle.epilogue_indexer(2, comp, w, 0.0, cs)
+        x = comp.astype(np.float64) * w
+        for b in range(4):
+            xb = x[32 * b:32 * b + 32]
+            amax = float(np.abs(xb).max())
+            ratio = Fraction(float(rn32_of_fraction(Fraction(amax) * inv6)))
+            e = math.ceil(math.log2(float(ratio)))
+            if Fraction(2) ** (e - 1) >= ratio:
+                e -= 1
+            assert e == ks[b] and sc[b] == e + 127
+            codes = [E2M1_MAG.index(abs(v) * 2.0 ** -e) | (8 if v < 0 else 0) for v in xb]
+            want = [codes[2 * j] | (codes[2 * j + 1] << 4) for j in range(16)]
+            assert list(tok[16 * b:16 * b + 16]) == want, b
+
+
+def test_forward_ex_matches_c128_forward():
+    """The generic op with the C128 configuration is the C128 op, byte for byte."""
+    p = inputs.make_problem("decode")
+    a = oracle.forward_k_cache(p)
+    b = p.k_cache.copy()
+    assert oracle.forward_ex(p, k_cache=b) == 0
+    assert np.array_equal(a, b)
+
+
+def test_overlap_gather_and_masking():
+    """Ratio 4 with overlap: 8 rows p-7..p; the older 4 read kv[0:H], score[SW:SW+H], the newer 4
+    read kv[H:2H], score[SW+H:SW+2H]; rows at negative positions take no weight. Identity-coded
+    kv + one-hot scores name the (block, row, half) each column read."""
+    for fmt, head in ((0, 512), (1, 128)):
+        p = inputs.prefill_problem("t", 3, 2, 12, 40, head, 4, 1, fmt)
+        sw = p.state_width
+        nb = p.state.shape[0]
+        code = (np.arange(nb)[:, None] * 8 + np.arange(8)[None, :]).astype(np.float32)
+        p.state[..., :sw] = code[..., None]
+        p.state[..., head:2 * head] += np.float32(0.5)            # marks the newer half
+        p.state[..., sw:] = -1000.0
+        rng = np.random.default_rng(fmt)
+        picks = {}
+        for t in range(p.num_tokens):
+            pos = int(p.positions[t])
+            if (pos + 1) % 4 or p.kv_slot_mapping[t] < 0:
+                continue
+            r = int(p.token_to_req[t])
+            valid = [i for i in range(8) if pos - 7 + i >= 0]
+            pick = rng.choice(valid, head)
+            picks[t] = pick
+            for c in range(head):
+                q = pos - 7 + pick[c]
+                ho = head if pick[c] >= 4 else 0
+                p.state[p.block_table[r, q // 8], q % 8, sw + ho + c] = 0.0
+        # windows share rows (overlap), so check one token at a time on a fresh copy of the scores
+        for t, pick in list(picks.items())[:12]:
+            q2 = p.state.copy()
+            pos, r = int(p.positions[t]), int(p.token_to_req[t])
+            q2[..., sw:] = -1000.0
+            for c in range(head):
+                q = pos - 7 + pick[c]
+                ho = head if pick[c] >= 4 else 0
+                q2[p.block_table[r, q // 8], q % 8, sw + ho + c] = 0.0
+            sub = inputs.Problem("x", p.token_to_req, p.positions, p.slot_mapping, p.block_table, q2, p.rms_w, p.eps,
+                                 p.cos_sin, p.k_cache, p.kv_slot_mapping, p.kv_block_size, head=head, ratio=4,
+                                 overlap=1, state_width=sw, fmt=fmt)
+            comp = np.zeros((p.num_tokens, head), np.float32)
+            oracle.forward_ex(sub, comp_out=comp, tokens=[t])
+            q = pos - 7 + pick
+            want = p.block_table[r, q // 8].astype(np.float32) * 8 + q % 8 + np.where(pick >= 4, 0.5, 0.0)
+            assert np.array_equal(comp[t], want.astype(np.float32)), t
