@@ -27,6 +27,7 @@ EXPORTS = (
     "compress_norm_rope_store",
     "c128_compress_norm_rope_store_debug",
     "c128_compress_norm_rope_store_noalloc",
+    "compress_norm_rope_store_ex",
     "c128_status_string",
     "c128_reserve_workspace",
     "c128_device_errors",
@@ -40,6 +41,20 @@ EXPORTS = (
 class Tensor(ctypes.Structure):
     _fields_ = [("data", ctypes.c_void_p), ("dtype", ctypes.c_int32), ("ndim", ctypes.c_int32),
                 ("shape", ctypes.c_int64 * 4), ("stride", ctypes.c_int64 * 4)]
+
+
+FORMAT_SPARSE_FP8, FORMAT_INDEXER_FP8, FORMAT_INDEXER_MXFP4 = 0, 1, 2
+
+
+class Config(ctypes.Structure):
+    """c128_config_t: head_dim, rope_head_dim, compress_ratio, overlap, state_width, cache_format."""
+    _fields_ = [("head_dim", ctypes.c_int32), ("rope_head_dim", ctypes.c_int32), ("compress_ratio", ctypes.c_int32),
+                ("overlap", ctypes.c_int32), ("state_width", ctypes.c_int32), ("cache_format", ctypes.c_int32)]
+
+
+def config(head_dim=512, compress_ratio=128, overlap=0, state_width=None, cache_format=0, rope_head_dim=64) -> Config:
+    sw = state_width if state_width is not None else head_dim * (1 + overlap)
+    return Config(head_dim, rope_head_dim, compress_ratio, overlap, sw, cache_format)
 
 
 class Info(ctypes.Structure):
@@ -76,6 +91,8 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     L.compress_norm_rope_store.argtypes = [T, T, T, T, T, T, ctypes.c_float, T, T, T, i64, vp]
     L.c128_compress_norm_rope_store_debug.argtypes = [T, T, T, T, T, T, ctypes.c_float, T, T, T, i64, T, vp]
     L.c128_compress_norm_rope_store_noalloc.argtypes = [T, T, T, T, T, T, ctypes.c_float, T, T, T, i64, vp]
+    L.compress_norm_rope_store_ex.argtypes = [ctypes.POINTER(Config), T, T, T, T, T, T, ctypes.c_float, T, T, T, i64,
+                                              T, vp]
     L.c128_status_string.argtypes = [ctypes.c_int]
     L.c128_status_string.restype = ctypes.c_char_p
     L.c128_reserve_workspace.argtypes = [i64, vp]
@@ -158,6 +175,21 @@ def compress_norm_rope_store(token_to_req_indices, positions, slot_mapping, bloc
         _check(rc, "c128_compress_norm_rope_store_debug")
 
 
+def compress_norm_rope_store_ex(cfg: Config, token_to_req_indices, positions, slot_mapping, block_table, state_cache,
+                                rms_w, eps: float, cos_sin_cache, k_cache, kv_slot_mapping, kv_block_size: int,
+                                stream=None, comp_out=None) -> None:
+    """The op for any configuration of the pages' fused kernels (see include/c128compress.h):
+    C4-style overlap, head-128 indexer caches in FP8 or MXFP4. ``comp_out`` ([T, head]) optional."""
+    L = lib()
+    descs = [describe(x) for x in (token_to_req_indices, positions, slot_mapping, block_table, state_cache, rms_w)]
+    cs, kc, kvs = describe(cos_sin_cache), describe(k_cache), describe(kv_slot_mapping)
+    co = describe(comp_out) if comp_out is not None else None
+    rc = L.compress_norm_rope_store_ex(ctypes.byref(cfg), *[ctypes.byref(a) for a in descs], ctypes.c_float(eps),
+                                       ctypes.byref(cs), ctypes.byref(kc), ctypes.byref(kvs), int(kv_block_size),
+                                       ctypes.byref(co) if co is not None else None, _stream_handle(stream))
+    _check(rc, "compress_norm_rope_store_ex")
+
+
 def compress_norm_rope_store_noalloc(token_to_req_indices, positions, slot_mapping, block_table, state_cache,
                                      rms_w, eps: float, cos_sin_cache, k_cache, kv_slot_mapping,
                                      kv_block_size: int, stream=None) -> None:
@@ -182,7 +214,7 @@ class PreparedCall:
 
     def __init__(self, token_to_req_indices, positions, slot_mapping, block_table, state_cache, rms_w, eps: float,
                  cos_sin_cache, k_cache, kv_slot_mapping, kv_block_size: int, stream=None, comp_out=None,
-                 noalloc: bool = False):
+                 noalloc: bool = False, cfg: Optional[Config] = None):
         L = lib()
         self._keep = (token_to_req_indices, positions, slot_mapping, block_table, state_cache, rms_w, cos_sin_cache,
                       k_cache, kv_slot_mapping, comp_out)
@@ -191,7 +223,12 @@ class PreparedCall:
         self._descs = (*d, cs, kc, kvs)
         args = [ctypes.byref(a) for a in d] + [ctypes.c_float(eps), ctypes.byref(cs), ctypes.byref(kc),
                                                ctypes.byref(kvs), ctypes.c_int64(int(kv_block_size))]
-        if comp_out is not None:
+        if cfg is not None:
+            self._cfg = cfg
+            self._co = describe(comp_out) if comp_out is not None else None
+            args = [ctypes.byref(self._cfg)] + args + [ctypes.byref(self._co) if self._co is not None else None]
+            self._fn, self._name = L.compress_norm_rope_store_ex, "compress_norm_rope_store_ex"
+        elif comp_out is not None:
             self._co = describe(comp_out)
             args.append(ctypes.byref(self._co))
             self._fn, self._name = L.c128_compress_norm_rope_store_debug, "c128_compress_norm_rope_store_debug"

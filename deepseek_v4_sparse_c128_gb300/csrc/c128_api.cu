@@ -122,10 +122,39 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
     if (rc_ != C128_OK) return rc_; \
   } while (0)
 
+// Bytes of token data and of scales per k_cache slot, per cache format.
+int64_t token_bytes(int fmt) { return fmt == C128_FORMAT_SPARSE_FP8 ? c128::kTokenStride : fmt == C128_FORMAT_INDEXER_FP8 ? 128 : 64; }
+int64_t scale_bytes(int fmt) { return fmt == C128_FORMAT_SPARSE_FP8 ? c128::kScaleDim : 4; }
+
+// Check a configuration of compress_norm_rope_store_ex (C128_ERR_UNSUPPORTED if the pages' kernels
+// have no such case).
+int check_config(const c128_config_t* c) {
+  if (c == nullptr) return C128_ERR_NULL_PTR;
+  if (c->rope_head_dim != c128::kRope) return C128_ERR_UNSUPPORTED;
+  if (c->cache_format == C128_FORMAT_SPARSE_FP8) {
+    if (c->head_dim != c128::kHead) return C128_ERR_UNSUPPORTED;
+  } else if (c->cache_format == C128_FORMAT_INDEXER_FP8 || c->cache_format == C128_FORMAT_INDEXER_MXFP4) {
+    if (c->head_dim != 128) return C128_ERR_UNSUPPORTED;
+  } else {
+    return C128_ERR_UNSUPPORTED;
+  }
+  if (c->overlap != 0 && c->overlap != 1) return C128_ERR_UNSUPPORTED;
+  const int r = c->compress_ratio;
+  if (r < 1 || (r & (r - 1)) != 0 || (1 + c->overlap) * r > 256) return C128_ERR_UNSUPPORTED;
+  if (c->state_width < (1 + c->overlap) * c->head_dim || c->state_width % 4 != 0) return C128_ERR_UNSUPPORTED;
+  return C128_OK;
+}
+
 int validate_call(const c128_tensor_t* ttr, const c128_tensor_t* pos, const c128_tensor_t* slot,
                   const c128_tensor_t* bt, const c128_tensor_t* state, const c128_tensor_t* rms_w, float eps,
                   const c128_tensor_t* cs, const c128_tensor_t* kc, const c128_tensor_t* kvslot,
-                  int64_t kv_block_size, const c128_tensor_t* comp_out, c128::Params* out) {
+                  int64_t kv_block_size, const c128_tensor_t* comp_out, c128::Params* out,
+                  const c128_config_t* cfg) {
+  // C128 unless a configuration is given
+  const c128_config_t c128_cfg = {c128::kHead, c128::kRope, c128::kRatio, 0, c128::kHead, C128_FORMAT_SPARSE_FP8};
+  if (cfg != nullptr) C128_TRY(check_config(cfg));
+  const c128_config_t& C = cfg != nullptr ? *cfg : c128_cfg;
+  const int64_t row_width = 2 * static_cast<int64_t>(C.state_width);
   // per-token vectors (the pages' token_to_req_indices, positions, slot_mapping, kv slot map)
   if (pos == nullptr) return C128_ERR_NULL_PTR;
   C128_TRY(check_desc(pos, C128_I64, 1));
@@ -140,17 +169,18 @@ int validate_call(const c128_tensor_t* ttr, const c128_tensor_t* pos, const c128
   if (bt->shape[1] > 1 && bt->stride[1] != 1) return C128_ERR_STRIDE;
   if (bt->shape[0] > 1 && bt->stride[0] < bt->shape[1]) return C128_ERR_STRIDE;
   C128_TRY(check_data(bt));
-  // state cache [NB, 8, 1024] fp32 (C128 layout: state block 8, row = kv 512 | score 512)
+  // state cache [NB, block, 2*state_width] fp32 (C128 layout: state block 8, row = kv 512 | score 512)
   C128_TRY(check_desc(state, C128_F32, 3));
-  if (state->shape[1] != c128::kStateBlock || state->shape[2] != c128::kRow) return C128_ERR_UNSUPPORTED;
+  if (cfg == nullptr && state->shape[1] != c128::kStateBlock) return C128_ERR_UNSUPPORTED;
+  if (state->shape[1] < 1 || state->shape[2] != row_width) return C128_ERR_UNSUPPORTED;
   if (state->stride[2] != 1) return C128_ERR_STRIDE;
-  if (state->stride[1] < c128::kRow || state->stride[0] < 1) return C128_ERR_STRIDE;
+  if (state->stride[1] < row_width || state->stride[0] < 1) return C128_ERR_STRIDE;
   if (state->stride[1] % 4 != 0 || state->stride[0] % 4 != 0 || !aligned(state->data, 16)) return C128_ERR_ALIGN;
   C128_TRY(check_data(state));
   if (state->shape[0] > 0x7fffffffLL) return C128_ERR_ARG;
-  // rms weight [512]
+  // rms weight [head]
   C128_TRY(check_desc(rms_w, C128_F32, 1));
-  if (rms_w->shape[0] != c128::kHead) return C128_ERR_UNSUPPORTED;
+  if (rms_w->shape[0] != C.head_dim) return C128_ERR_UNSUPPORTED;
   if (rms_w->stride[0] != 1) return C128_ERR_STRIDE;
   C128_TRY(check_data(rms_w));
   if (!aligned(rms_w->data, 8)) return C128_ERR_ALIGN;
@@ -159,19 +189,19 @@ int validate_call(const c128_tensor_t* ttr, const c128_tensor_t* pos, const c128
   if (cs->shape[1] != c128::kRope) return C128_ERR_UNSUPPORTED;
   if (cs->stride[1] != 1 || (cs->shape[0] > 1 && cs->stride[0] < c128::kRope)) return C128_ERR_STRIDE;
   C128_TRY(check_data(cs));
-  // k_cache [NKB, bs, W] uint8, W >= 584; block b is a flat byte range of stride[0] bytes
+  // k_cache [NKB, bs, W] uint8, W >= slot bytes (584 for C128); block b is a flat byte range
   C128_TRY(check_desc(kc, C128_U8, 3));
   if (kv_block_size < 1 || kc->shape[1] != kv_block_size) return C128_ERR_ARG;
-  if (kc->shape[2] < c128::kSlotBytes) return C128_ERR_SHAPE;
+  if (kc->shape[2] < token_bytes(C.cache_format) + scale_bytes(C.cache_format)) return C128_ERR_SHAPE;
   if (kc->stride[2] != 1 || kc->stride[1] != kc->shape[2]) return C128_ERR_STRIDE;
   if (kc->shape[0] > 1 && kc->stride[0] < kc->shape[1] * kc->shape[2]) return C128_ERR_STRIDE;
   if (kc->stride[0] % 8 != 0 || !aligned(kc->data, 16)) return C128_ERR_ALIGN;
   C128_TRY(check_data(kc));
-  // optional fp32 export [T, 512]
+  // optional fp32 export [T, head]
   if (comp_out != nullptr) {
     C128_TRY(check_desc(comp_out, C128_F32, 2));
-    if (comp_out->shape[0] != T || comp_out->shape[1] != c128::kHead) return C128_ERR_SHAPE;
-    if (comp_out->stride[1] != 1 || (T > 1 && comp_out->stride[0] != c128::kHead)) return C128_ERR_STRIDE;
+    if (comp_out->shape[0] != T || comp_out->shape[1] != C.head_dim) return C128_ERR_SHAPE;
+    if (comp_out->stride[1] != 1 || (T > 1 && comp_out->stride[0] != C.head_dim)) return C128_ERR_STRIDE;
     C128_TRY(check_data(comp_out));
     if (!aligned(comp_out->data, 8)) return C128_ERR_ALIGN;
   }
@@ -200,15 +230,22 @@ int validate_call(const c128_tensor_t* ttr, const c128_tensor_t* pos, const c128
   p.kv_bs = kv_block_size;
   p.kc_stride0 = kc->shape[0] > 1 ? kc->stride[0] : kc->shape[1] * kc->shape[2];
   p.comp_out = comp_out != nullptr ? static_cast<float*>(comp_out->data) : nullptr;
+  p.head = C.head_dim;
+  p.ratio = C.compress_ratio;
+  p.overlap = C.overlap;
+  p.sw = C.state_width;
+  p.fmt = C.cache_format;
+  p.sblk = state->shape[1];
   return C128_OK;
 }
 
 int run(const c128_tensor_t* ttr, const c128_tensor_t* pos, const c128_tensor_t* slot,
         const c128_tensor_t* bt, const c128_tensor_t* state, const c128_tensor_t* rms_w, float eps,
         const c128_tensor_t* cs, const c128_tensor_t* kc, const c128_tensor_t* kvslot,
-        int64_t kv_block_size, const c128_tensor_t* comp_out, cudaStream_t stream) {
+        int64_t kv_block_size, const c128_tensor_t* comp_out, cudaStream_t stream,
+        const c128_config_t* config = nullptr) {
   c128::Params p{};
-  C128_TRY(validate_call(ttr, pos, slot, bt, state, rms_w, eps, cs, kc, kvslot, kv_block_size, comp_out, &p));
+  C128_TRY(validate_call(ttr, pos, slot, bt, state, rms_w, eps, cs, kc, kvslot, kv_block_size, comp_out, &p, config));
   const int64_t T = p.T;
   if (T == 0) return C128_OK;
 
@@ -248,8 +285,8 @@ namespace c128 {
 int validate_args(const c128_tensor_t* ttr, const c128_tensor_t* pos, const c128_tensor_t* slot,
                   const c128_tensor_t* bt, const c128_tensor_t* state, const c128_tensor_t* rms_w, float eps,
                   const c128_tensor_t* cs, const c128_tensor_t* kc, const c128_tensor_t* kvslot,
-                  int64_t kv_block_size, const c128_tensor_t* comp_out, Params* out) {
-  return validate_call(ttr, pos, slot, bt, state, rms_w, eps, cs, kc, kvslot, kv_block_size, comp_out, out);
+                  int64_t kv_block_size, const c128_tensor_t* comp_out, Params* out, const c128_config_t* cfg) {
+  return validate_call(ttr, pos, slot, bt, state, rms_w, eps, cs, kc, kvslot, kv_block_size, comp_out, out, cfg);
 }
 }  // namespace c128
 
@@ -279,6 +316,17 @@ int c128_compress_norm_rope_store_debug(const c128_tensor_t* token_to_req_indice
              reinterpret_cast<cudaStream_t>(stream));
 }
 
+int compress_norm_rope_store_ex(const c128_config_t* config, const c128_tensor_t* token_to_req_indices,
+                                const c128_tensor_t* positions, const c128_tensor_t* slot_mapping,
+                                const c128_tensor_t* block_table, const c128_tensor_t* state_cache,
+                                const c128_tensor_t* rms_w, float eps, const c128_tensor_t* cos_sin_cache,
+                                const c128_tensor_t* k_cache, const c128_tensor_t* kv_slot_mapping,
+                                int64_t kv_block_size, const c128_tensor_t* comp_out, c128_stream_t stream) {
+  if (config == nullptr) return C128_ERR_NULL_PTR;
+  return run(token_to_req_indices, positions, slot_mapping, block_table, state_cache, rms_w, eps, cos_sin_cache,
+             k_cache, kv_slot_mapping, kv_block_size, comp_out, reinterpret_cast<cudaStream_t>(stream), config);
+}
+
 const char* c128_status_string(int status) {
   switch (status) {
     case C128_OK: return "ok";
@@ -287,7 +335,8 @@ const char* c128_status_string(int status) {
     case C128_ERR_SHAPE: return "wrong shape";
     case C128_ERR_STRIDE: return "unsupported stride";
     case C128_ERR_ALIGN: return "misaligned base or stride";
-    case C128_ERR_UNSUPPORTED: return "not the C128 layout (state block 8, row 1024, head 512, rope 64)";
+    case C128_ERR_UNSUPPORTED:
+      return "unsupported configuration or layout (C128: state block 8, row 1024, head 512, rope 64)";
     case C128_ERR_ARG: return "bad argument (kv_block_size must equal k_cache.shape[1]; too many tokens)";
     case C128_ERR_CUDA: return "CUDA error";
     case C128_ERR_NOMEM: return "workspace allocation failed";

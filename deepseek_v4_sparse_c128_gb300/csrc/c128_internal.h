@@ -60,9 +60,22 @@ struct Params {
   int64_t cs_rows, cs_stride;
   uint8_t* kc;
   int64_t nkb, kv_bs, kc_stride0;  // blocks, block size, block stride in bytes
-  float* comp_out;            // nullable [T, 512]
+  float* comp_out;            // nullable [T, head]
   WsHeader* ws;               // header; the token list follows it
+  // configuration (C128: head 512, ratio 128, no overlap, state width 512, format 0, block 8)
+  int32_t head;               // 512 or 128
+  int32_t ratio;              // compress ratio (a power of two)
+  int32_t overlap;            // 1: windows of 2*ratio rows, the newer half read at +head
+  int32_t sw;                 // state width: kv columns of a row, as many score columns follow
+  int32_t fmt;                // cache format (C128_FORMAT_*)
+  int64_t sblk;               // state-cache block size (rows per block)
 };
+
+// True for the configuration the specialised C128 kernels serve.
+inline bool is_c128(const Params& p) {
+  return p.head == kHead && p.ratio == kRatio && p.overlap == 0 && p.sw == kHead && p.fmt == 0 &&
+         p.sblk == kStateBlock;
+}
 
 struct LaunchCfg {
   int sm_count;
@@ -73,13 +86,17 @@ struct LaunchCfg {
 };
 
 // Check every argument of compress_norm_rope_store (C128_* code) and fill all of `out` but `ws`.
+// `cfg` == nullptr means the C128 configuration (state block 8 required).
 int validate_args(const c128_tensor_t* ttr, const c128_tensor_t* pos, const c128_tensor_t* slot,
                   const c128_tensor_t* bt, const c128_tensor_t* state, const c128_tensor_t* rms_w, float eps,
                   const c128_tensor_t* cs, const c128_tensor_t* kc, const c128_tensor_t* kvslot,
-                  int64_t kv_block_size, const c128_tensor_t* comp_out, Params* out);
+                  int64_t kv_block_size, const c128_tensor_t* comp_out, Params* out,
+                  const c128_config_t* cfg = nullptr);
 
 // Enqueue zeroing of the per-call counters, the planning kernel and the compress kernel.
 cudaError_t launch(const Params& p, const LaunchCfg& cfg, cudaStream_t stream);
+// The kernel for configurations other than C128 (after plan_kernel; see c128_gather.cu).
+cudaError_t launch_gather(const Params& p, const LaunchCfg& cfg, cudaStream_t stream);
 int compress_smem_bytes();
 cudaError_t prepare_device(int device);  // one-time function attributes
 

@@ -194,6 +194,59 @@ int c128_compress_norm_rope_store_noalloc(const c128_tensor_t* token_to_req_indi
                                           int64_t kv_block_size,
                                           c128_stream_t stream);
 
+/*
+ * compress_norm_rope_store_ex — the same op for the other configurations of the fused kernels
+ * on the API page (one launcher, compress_norm_rope_store_triton, serves all three):
+ *
+ *   C128_FORMAT_SPARSE_FP8    _fused_kv_compress_norm_rope_insert_sparse_attn: head 512, rope 64;
+ *                             448 e4m3 + 64 bf16 rope (576 B) then 8 scale bytes per slot
+ *   C128_FORMAT_INDEXER_FP8   _fused_kv_compress_norm_rope_insert_indexer_attn: head 128, rope 64;
+ *                             RoPE of the last 32 pairs first, bf16 round, one absmax block:
+ *                             128 e4m3 bytes per slot, then one fp32 scale 2^e (4 B) per slot
+ *   C128_FORMAT_INDEXER_MXFP4 _fused_kv_compress_norm_rope_insert_indexer_mxfp4_attn: head 128;
+ *                             RoPE, bf16 round, per 32 values e = ceil(log2(absmax/6)) (absmax
+ *                             floor 6*2^-126, e clamped to [-127,127]), E2M1 codes of x*2^-e
+ *                             (round to nearest even, saturating), pair j in byte j with the even
+ *                             value in the low nibble: 64 bytes per slot, then 4 UE8M0 bytes (e+127)
+ *
+ * with compress ratio `compress_ratio` (a power of two; window end: (p+1) % ratio == 0) and, when
+ * `overlap` is 1, windows of 2*ratio rows whose newer `ratio` rows read kv and score at +head_dim
+ * (the C4 layout); rows at negative positions take no weight. A state row is kv[state_width]
+ * followed by score[state_width] (state_width >= (1+overlap)*head_dim, a multiple of 4), blocks of
+ * any number of rows (state_cache [NB, block, 2*state_width]); cos/sin come from row
+ * (p / ratio) * ratio. k_cache blocks hold bs token records then bs scale records, as above.
+ * comp_out, if not NULL, receives the fp32 compressed vectors ([T, head_dim]) of stored tokens.
+ * Everything else is as for compress_norm_rope_store; the C128 configuration (512, 64, 128, 0, 512,
+ * sparse, state block 8) runs the same kernels as compress_norm_rope_store.
+ */
+enum {
+    C128_FORMAT_SPARSE_FP8 = 0,
+    C128_FORMAT_INDEXER_FP8 = 1,
+    C128_FORMAT_INDEXER_MXFP4 = 2,
+};
+typedef struct c128_config {
+    int32_t head_dim;        /* 512 (sparse format) or 128 (indexer formats) */
+    int32_t rope_head_dim;   /* 64 */
+    int32_t compress_ratio;  /* power of two; (1 + overlap) * ratio <= 256 */
+    int32_t overlap;         /* 0 or 1 */
+    int32_t state_width;     /* kv columns of a state row; as many score columns follow */
+    int32_t cache_format;    /* C128_FORMAT_* */
+} c128_config_t;
+int compress_norm_rope_store_ex(const c128_config_t* config,
+                                const c128_tensor_t* token_to_req_indices,
+                                const c128_tensor_t* positions,
+                                const c128_tensor_t* slot_mapping,
+                                const c128_tensor_t* block_table,
+                                const c128_tensor_t* state_cache,
+                                const c128_tensor_t* rms_w,
+                                float eps,
+                                const c128_tensor_t* cos_sin_cache,
+                                const c128_tensor_t* k_cache,
+                                const c128_tensor_t* kv_slot_mapping,
+                                int64_t kv_block_size,
+                                const c128_tensor_t* comp_out,
+                                c128_stream_t stream);
+
 /* Human-readable name of a return code (static string, never NULL). */
 const char* c128_status_string(int status);
 

@@ -174,3 +174,80 @@ def slots_agree(problem, kc_a, kc_b, rows):
         max_rope = max(max_rope, float(dr.max()))
     assert np.array_equal(fa[~inside], fb[~inside]), "bytes outside the stored slots differ"
     return differ, max_deq, max_rope
+
+
+# ------------------------------------------------------------ other configurations (the _ex call)
+FORMAT_BYTES = {0: (576, 8), 1: (128, 4), 2: (64, 4)}
+
+
+def run_gpu_ex(problem, dev=None, comp=True, stream=None):
+    """Run compress_norm_rope_store_ex with the problem's configuration."""
+    import torch
+    from deepseek_v4_sparse_c128_gb300 import binding
+    dev = dev or to_device(problem)
+    T, head = problem.num_tokens, problem.head
+    comp_out = None
+    if comp:
+        comp_out = torch.full((T, head), NAN_BITS, dtype=torch.int32, device=dev["state"].device).view(torch.float32)
+    cfg = binding.config(problem.head, problem.ratio, problem.overlap, problem.state_width, problem.fmt)
+    binding.compress_norm_rope_store_ex(cfg, dev["token_to_req"], dev["positions"], dev["slot_mapping"],
+                                        dev["block_table"], dev["state"], dev["rms_w"], problem.eps, dev["cos_sin"],
+                                        dev["k_cache"], dev["kv_slot_mapping"], problem.kv_block_size, stream=stream,
+                                        comp_out=comp_out)
+    torch.cuda.synchronize()
+    err = binding.device_errors(stream, clear=True)
+    return dev["k_cache"].cpu().numpy(), (comp_out.cpu().numpy() if comp else None), err
+
+
+def slot_ranges_ex(problem, t):
+    tb, sb = FORMAT_BYTES[problem.fmt]
+    s = int(problem.kv_slot_mapping[t])
+    bs = problem.kv_block_size
+    stride = problem.k_cache.shape[1] * problem.k_cache.shape[2]
+    blk, off = divmod(s, bs)
+    tok = blk * stride + off * tb
+    scl = blk * stride + bs * tb + off * sb
+    return slice(tok, tok + tb), slice(scl, scl + sb)
+
+
+def replay_expected_ex(problem, comp, rows):
+    kc = problem.k_cache.copy()
+    flat = kc.reshape(-1)
+    for t in rows:
+        p = int(problem.positions[t])
+        row = problem.cos_sin[(p // problem.ratio) * problem.ratio]
+        if problem.fmt == 0:
+            tok, sc = oracle.epilogue(comp[t], problem.rms_w, problem.eps, row)
+        else:
+            tok, sc = oracle.epilogue_indexer(problem.fmt, comp[t], problem.rms_w, problem.eps, row)
+        a, b = slot_ranges_ex(problem, t)
+        flat[a] = tok
+        flat[b] = sc
+    return kc
+
+
+def check_against_oracle_ex(problem, kc_gpu, comp_gpu, threads=8):
+    """Two-level parity for any configuration: same stored tokens as the oracle, comp32 within
+    1e-6 + 1e-5|x|, and every k_cache byte equal to the oracle epilogue replayed on the GPU's
+    comp32; bytes that differ from the oracle's own output are counted."""
+    T, head = problem.num_tokens, problem.head
+    comp_ref = np.zeros((T, head), np.float32)
+    comp_ref.view(np.uint32)[:] = NAN_BITS
+    kc_ref = problem.k_cache.copy()
+    err_ref = oracle.forward_ex(problem, k_cache=kc_ref, comp_out=comp_ref, threads=threads)
+    rows_ref, rows_gpu = written_rows(comp_ref), written_rows(comp_gpu)
+    assert np.array_equal(rows_ref, rows_gpu), "the set of stored tokens differs from the oracle's"
+    ok, max_abs, worst = comp_close(comp_gpu[rows_ref], comp_ref[rows_ref])
+    assert ok, f"compressed vector outside 1e-6 + 1e-5|x|: max abs {max_abs:.3g}, worst/tol {worst:.3g}"
+    kc_replay = replay_expected_ex(problem, comp_gpu, rows_ref)
+    diff = np.nonzero(kc_replay.reshape(-1) != kc_gpu.reshape(-1))[0]
+    assert diff.size == 0, f"{diff.size} bytes differ from the oracle epilogue replay (first at {diff[:8]})"
+    d2 = kc_ref.reshape(-1) != kc_gpu.reshape(-1)
+    windows = 0
+    for t in rows_ref:
+        a, b = slot_ranges_ex(problem, t)
+        if d2[a].any() or d2[b].any():
+            windows += 1
+            assert not np.array_equal(comp_gpu[t].view(np.uint32), comp_ref[t].view(np.uint32))
+    return {"stored": int(rows_ref.size), "comp_max_abs": max_abs, "comp_worst_over_tol": worst,
+            "oracle_err_bits": err_ref, "e2e_bytes_differ": int(d2.sum()), "e2e_windows_differ": windows}

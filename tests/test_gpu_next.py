@@ -1,0 +1,137 @@
+"""CUDA path vs the CPU oracle for the other configurations of the pages' fused kernels, through
+compress_norm_rope_store_ex: C4 overlapping windows with the sparse-attention cache (head 512),
+and the head-128 indexer with an FP8 (fp32 scale) or MXFP4 (UE8M0) cache at compress ratios 4
+(overlap) and 128. Same two-level parity as the C128 tests."""
+import numpy as np
+import pytest
+
+import oracle
+from deepseek_v4_sparse_c128_gb300 import inputs
+from gpu_util import (check_against_oracle_ex, run_gpu, run_gpu_ex, to_device, written_rows)
+
+pytestmark = pytest.mark.gpu
+
+NEXT = ["c4_sparse", "idx_c4_fp8", "idx_c4_mxfp4", "idx_c128_fp8", "idx_c128_mxfp4"]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from deepseek_v4_sparse_c128_gb300 import build, binding
+    build.build()
+    binding.load()
+
+
+@pytest.mark.parametrize("name", NEXT)
+def test_next_workload_parity(name):
+    p = inputs.make_next_problem(name)
+    kc, comp, err = run_gpu_ex(p)
+    assert err == 0
+    rep = check_against_oracle_ex(p, kc, comp, threads=16)
+    print(name, rep)
+    assert rep["stored"] > 100
+
+
+@pytest.mark.parametrize("block", [1, 4, 16, 32])
+@pytest.mark.parametrize("fmt,head", [(0, 512), (2, 128)])
+def test_other_state_block_sizes(block, fmt, head):
+    p = inputs.prefill_problem("blk", 11 + block, 6, 5, 300, head, 4, 1, fmt, state_block=block, kv_block_size=16,
+                               decode_tail=5)
+    kc, comp, err = run_gpu_ex(p)
+    assert err == 0
+    check_against_oracle_ex(p, kc, comp, threads=16)
+
+
+def test_c128_config_through_ex_is_the_c128_call():
+    for name in ("decode", "mixed"):
+        p = inputs.make_problem(name)
+        a, ca, _ = run_gpu(p)
+        b, cb, _ = run_gpu_ex(p)
+        assert np.array_equal(a, b)
+        rows = written_rows(ca)
+        assert np.array_equal(ca[rows].view(np.uint32), cb[rows].view(np.uint32))
+
+
+def test_c128_config_with_other_block_size_uses_generic_path():
+    """C128 sizes with a state block of 16 rows: the generic kernel, checked against the oracle."""
+    p = inputs.prefill_problem("c128b16", 5, 3, 128, 3000, 512, 128, 0, 0, state_block=16, decode_tail=20)
+    kc, comp, err = run_gpu_ex(p)
+    assert err == 0
+    check_against_oracle_ex(p, kc, comp, threads=16)
+
+
+@pytest.mark.parametrize("name", ["idx_c4_fp8", "c4_sparse"])
+def test_bad_indices_generic_path(name):
+    p = inputs.make_next_problem(name)
+    act = [t for t in range(p.num_tokens) if p.kv_slot_mapping[t] >= 0 and p.positions[t] >= 7]
+    t_req, t_blk, t_kv, t_bt = act[3], act[10], act[20], act[30]
+    p.token_to_req[t_req] = p.block_table.shape[0]
+    r = int(p.token_to_req[t_blk])
+    q = int(p.positions[t_blk]) - 2
+    p.block_table[r, q // p.state.shape[1]] = p.state.shape[0]
+    p.kv_slot_mapping[t_kv] = p.k_cache.shape[0] * p.kv_block_size
+    p.positions[t_bt] = p.block_table.shape[1] * p.state.shape[1] + 3
+    kc, comp, err = run_gpu_ex(p)
+    ref = p.k_cache.copy()
+    err_ref = oracle.forward_ex(p, k_cache=ref)
+    assert err == err_ref and err & (1 | 2 | 4 | 16) == (1 | 2 | 4 | 16)
+    rep = check_against_oracle_ex(p, kc, comp)
+    assert not {t_req, t_blk, t_kv, t_bt} & set(written_rows(comp).tolist())
+    assert rep["stored"] > 0
+
+
+@pytest.mark.parametrize("fmt,head", [(1, 128), (2, 128), (0, 512)])
+def test_one_hot_epilogue_edges_generic(fmt, head):
+    """One-hot scores (0 on one valid row, -1000 elsewhere) make comp32 equal crafted kv values on
+    both sides: wide dynamic range (slow exact variance), subnormals, zeros, E2M1/e4m3 ties,
+    tiny blocks (MXFP4 scale near 2^-127), an overflowing variance."""
+    p = inputs.prefill_problem("onehot", 21, 4, 8, 64, head, 4, 1, fmt, decode_tail=8)
+    rng = np.random.default_rng(fmt)
+    sw = p.state_width
+    p.state[..., sw:] = -1000.0
+    rows_tok = [t for t in range(p.num_tokens) if p.kv_slot_mapping[t] >= 0]
+    want = {}
+    for n, t in enumerate(rows_tok):
+        kind = n % 8
+        if kind == 0:
+            v = rng.standard_normal(head) * 2.0 ** rng.integers(-60, 40, head)
+        elif kind == 1:
+            v = rng.standard_normal(head) * 1e-40
+        elif kind == 2:
+            v = np.zeros(head)
+        elif kind == 3:
+            v = rng.choice([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, -0.25, -2.5], head) * 2.0 ** rng.integers(-3, 3)
+        elif kind == 4:
+            v = rng.standard_normal(head) * 1e25
+        elif kind == 5:
+            v = rng.standard_normal(head) * 1e-30
+        else:
+            v = rng.standard_normal(head)
+        pos, r = int(p.positions[t]), int(p.token_to_req[t])
+        valid = [i for i in range(8) if pos - 7 + i >= 0]
+        pick = rng.choice(valid, head)
+        for c in range(head):
+            q = pos - 7 + pick[c]
+            ho = head if pick[c] >= 4 else 0
+            b, o = p.block_table[r, q // 8], q % 8
+            p.state[b, o, sw + ho + c] = 0.0
+            p.state[b, o, ho + c] = np.float32(v[c])
+        want[t] = v.astype(np.float32)
+    kc, comp, err = run_gpu_ex(p)
+    assert err == 0
+    for t, v in want.items():
+        assert np.array_equal(comp[t].view(np.uint32), v.view(np.uint32)), t
+    rep = check_against_oracle_ex(p, kc, comp)
+    assert rep["e2e_bytes_differ"] == 0
+
+
+def test_padded_strides_generic():
+    import torch
+    p = inputs.make_next_problem("idx_c4_mxfp4")
+    dev = to_device(p)
+    NB, BS, RW = p.state.shape
+    big = torch.zeros((NB, BS, RW + 36), dtype=torch.float32, device="cuda")
+    big[:, :, :RW].copy_(dev["state"])
+    dev["state"] = big[:, :, :RW]
+    kc, comp, err = run_gpu_ex(p, dev=dev)
+    assert err == 0
+    check_against_oracle_ex(p, kc, comp)
