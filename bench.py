@@ -324,6 +324,8 @@ def run_ours(args, ws, rank, local):
         out["cpu_baseline"] = {"value": wps, "unit": UNIT, "cores": threads, "kind": "oracle",
                                "sample": f"{sample.size} random windows of sweep{T} x {passes} passes "
                                          f"({cpu_s:.1f} s CPU), oracle over host threads"}
+    if not args.no_next and ws == 1:
+        out["other_configurations"] = bench_next(args, dev)
     if not args.no_sweep and ws == 1:
         del d, p
         torch.cuda.empty_cache()
@@ -409,6 +411,59 @@ def sweep(args, dev):
     return {"eager": eager, "graph": graph, "rotate4_no_flush": rot4}
 
 
+def bench_next(args, dev):
+    """The other configurations of the pages' fused kernels through compress_norm_rope_store_ex
+    (C4 overlap with the sparse-attention cache; the head-128 indexer with FP8 or MXFP4 caches at
+    ratios 4 and 128), each on a prefill batch with about a quarter million tokens whose state is
+    larger than L2: µs per call, windows/s, and the gather kernel's algorithmic GB/s."""
+    import torch
+    from deepseek_v4_sparse_c128_gb300 import binding
+    peaks = {}
+    try:
+        peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+    except (OSError, ValueError):
+        pass
+    peak = float(peaks.get("hbm_gbs", 6800.0))
+    res = {}
+    for name, scale in (("c4_sparse", 64), ("idx_c4_fp8", 64), ("idx_c4_mxfp4", 64), ("idx_c128_fp8", 16),
+                        ("idx_c128_mxfp4", 16)):
+        p = inputs.make_next_problem(name, state_device=str(dev), scale=scale)
+        to = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+        d = {k: to(getattr(p, k)) for k in ("token_to_req", "positions", "slot_mapping", "block_table", "rms_w",
+                                            "cos_sin", "k_cache", "kv_slot_mapping")}
+        cfg = binding.config(p.head, p.ratio, p.overlap, p.state_width, p.fmt)
+        stream = torch.cuda.current_stream()
+        call = binding.PreparedCall(d["token_to_req"], d["positions"], d["slot_mapping"], d["block_table"], p.state,
+                                    d["rms_w"], p.eps, d["cos_sin"], d["k_cache"], d["kv_slot_mapping"],
+                                    p.kv_block_size, stream=stream, cfg=cfg)
+        binding.reserve_workspace(p.num_tokens)
+        for _ in range(3):
+            call()
+        torch.cuda.synchronize()
+        n = 20
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with binding.KernelTimer() as kt:
+            a.record(stream)
+            for _ in range(n):
+                call()
+            b.record(stream)
+            torch.cuda.synchronize()
+        assert binding.device_errors(clear=True) == 0
+        A = int(((p.positions + 1) % p.ratio == 0).sum())   # every token here has a slot; window ends
+        rows = (1 + p.overlap) * p.ratio
+        tb, sb = {0: (576, 8), 1: (128, 4), 2: (64, 4)}[p.fmt]
+        per_window = rows * 2 * p.head * 4 + rows * 4 + 256 + tb + sb
+        kus = kt.total_ms * 1e3 / kt.launches
+        achieved = A * per_window / (kus * 1e-6) / 1e9
+        res[name] = {"tokens": p.num_tokens, "windows": A, "us_per_call": round(a.elapsed_time(b) * 1e3 / n, 2),
+                     "windows_per_s": A / (a.elapsed_time(b) / n * 1e-3), "kernel_us": round(kus, 2),
+                     "algorithmic_bytes_per_window": per_window, "achieved_gbs": round(achieved, 1),
+                     "frac_of_measured_hbm": round(achieved / peak, 3)}
+        del d, p, call
+        torch.cuda.empty_cache()
+    return res
+
+
 # --------------------------------------------------------------------------- reference arm
 def run_reference(args, ws, rank):
     """The CPU oracle as it stands, on the host cores, over a bounded sample of the same workload."""
@@ -453,6 +508,7 @@ def main():
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-next", action="store_true")
     args = ap.parse_args()
     ws, rank, local = dist_setup()
     try:

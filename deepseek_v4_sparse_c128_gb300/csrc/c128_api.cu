@@ -203,7 +203,7 @@ int validate_call(const c128_tensor_t* ttr, const c128_tensor_t* pos, const c128
     if (comp_out->shape[0] != T || comp_out->shape[1] != C.head_dim) return C128_ERR_SHAPE;
     if (comp_out->stride[1] != 1 || (T > 1 && comp_out->stride[0] != C.head_dim)) return C128_ERR_STRIDE;
     C128_TRY(check_data(comp_out));
-    if (!aligned(comp_out->data, 8)) return C128_ERR_ALIGN;
+    if (!aligned(comp_out->data, 16)) return C128_ERR_ALIGN;
   }
   c128::Params& p = *out;
   p = c128::Params{};

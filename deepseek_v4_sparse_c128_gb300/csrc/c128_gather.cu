@@ -12,6 +12,8 @@
 // shared memory and are merged in row-group order. The 512-wide format then runs the shared
 // fused epilogue; the indexer formats run a 64-thread epilogue (RMSNorm, RoPE of the last 32
 // pairs, bf16 round, then FP8 with one fp32 scale or MXFP4 with a UE8M0 byte per 32 values).
+#include <cstddef>
+
 #include "c128_device.cuh"
 
 namespace c128 {
@@ -45,6 +47,11 @@ struct GatherSmem {
   EpiSmem epi;
   IdxSmem idx;
 };
+
+static_assert(sizeof(float) * GatherGeo<512>::kRowGroups * 512 % 16 == 0 &&
+                  sizeof(float) * GatherGeo<128>::kRowGroups * 128 % 16 == 0,
+              "float4 access to the partial arrays");
+static_assert(offsetof(IdxSmem, comp) % 8 == 0, "float2 access to IdxSmem::comp");
 
 __device__ __forceinline__ void idx_bar() { asm volatile("bar.sync 2, %0;" ::"n"(kIdxThreads) : "memory"); }
 

@@ -95,8 +95,11 @@ int validate_args(const c128_tensor_t* ttr, const c128_tensor_t* pos, const c128
 
 // Enqueue zeroing of the per-call counters, the planning kernel and the compress kernel.
 cudaError_t launch(const Params& p, const LaunchCfg& cfg, cudaStream_t stream);
-// The kernel for configurations other than C128 (after plan_kernel; see c128_gather.cu).
+// The kernels for configurations other than C128 (after plan_kernel): windows of at most 8 rows
+// (c128_c4.cu) and the rest (c128_gather.cu).
 cudaError_t launch_gather(const Params& p, const LaunchCfg& cfg, cudaStream_t stream);
+bool small_window_path(const Params& p);
+cudaError_t launch_small(const Params& p, const LaunchCfg& cfg, cudaStream_t stream);
 int compress_smem_bytes();
 cudaError_t prepare_device(int device);  // one-time function attributes
 

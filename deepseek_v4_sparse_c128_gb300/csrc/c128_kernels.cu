@@ -556,7 +556,8 @@ cudaError_t launch(const Params& p, const LaunchCfg& cfg, cudaStream_t stream) {
     plan_kernel<<<plan_grid, kPlanThreads, 0, stream>>>(p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (cfg.ev_begin != nullptr && (e = cudaEventRecord(cfg.ev_begin, stream)) != cudaSuccess) return e;
-    if ((e = launch_gather(p, cfg, stream)) != cudaSuccess) return e;
+    e = small_window_path(p) ? launch_small(p, cfg, stream) : launch_gather(p, cfg, stream);
+    if (e != cudaSuccess) return e;
     if (cfg.ev_end != nullptr) e = cudaEventRecord(cfg.ev_end, stream);
     return e;
   }

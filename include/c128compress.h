@@ -141,7 +141,7 @@ int compress_norm_rope_store(const c128_tensor_t* token_to_req_indices,
 /*
  * Same as compress_norm_rope_store, and also writes the fp32 compressed vector (the softmax-
  * weighted sum, before RMSNorm) of every token it stores to comp_out [T, 512] fp32 (contiguous,
- * 8-byte aligned). Rows of other tokens are left as they were. For tests and diagnostics: it
+ * 16-byte aligned). Rows of other tokens are left as they were. For tests and diagnostics: it
  * exposes the quantity the byte-exact epilogue is a function of.
  */
 int c128_compress_norm_rope_store_debug(const c128_tensor_t* token_to_req_indices,
@@ -215,7 +215,8 @@ int c128_compress_norm_rope_store_noalloc(const c128_tensor_t* token_to_req_indi
  * followed by score[state_width] (state_width >= (1+overlap)*head_dim, a multiple of 4), blocks of
  * any number of rows (state_cache [NB, block, 2*state_width]); cos/sin come from row
  * (p / ratio) * ratio. k_cache blocks hold bs token records then bs scale records, as above.
- * comp_out, if not NULL, receives the fp32 compressed vectors ([T, head_dim]) of stored tokens.
+ * comp_out, if not NULL, receives the fp32 compressed vectors ([T, head_dim], contiguous, 16-byte
+ * aligned) of stored tokens.
  * Everything else is as for compress_norm_rope_store; the C128 configuration (512, 64, 128, 0, 512,
  * sparse, state block 8) runs the same kernels as compress_norm_rope_store.
  */

@@ -142,6 +142,16 @@ def test_validation_codes(L, case, code):
     assert _call(L, a) == code
 
 
+def test_misaligned_comp_out_is_rejected(L):
+    a = _args(T=5)
+    r = ctypes.byref
+    comp = _t([5, 512], binding.C128_F32, data=FAKE + 8)
+    rc = L.c128_compress_norm_rope_store_debug(r(a["ttr"]), r(a["pos"]), r(a["slot"]), r(a["bt"]), r(a["state"]),
+                                               r(a["rms"]), ctypes.c_float(1e-6), r(a["cs"]), r(a["kc"]),
+                                               r(a["kvs"]), 2, r(comp), None)
+    assert rc == 5
+
+
 def test_debug_entry_requires_comp_out(L):
     a = _args(T=0)
     r = ctypes.byref

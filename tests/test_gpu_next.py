@@ -79,12 +79,16 @@ def test_bad_indices_generic_path(name):
     assert rep["stored"] > 0
 
 
-@pytest.mark.parametrize("fmt,head", [(1, 128), (2, 128), (0, 512)])
-def test_one_hot_epilogue_edges_generic(fmt, head):
+@pytest.mark.parametrize("fmt,head,ratio,overlap", [(1, 128, 4, 1), (2, 128, 4, 1), (0, 512, 4, 1),
+                                                   (1, 128, 128, 0), (2, 128, 128, 0), (2, 128, 16, 1)])
+def test_one_hot_epilogue_edges_generic(fmt, head, ratio, overlap):
     """One-hot scores (0 on one valid row, -1000 elsewhere) make comp32 equal crafted kv values on
     both sides: wide dynamic range (slow exact variance), subnormals, zeros, E2M1/e4m3 ties,
-    tiny blocks (MXFP4 scale near 2^-127), an overflowing variance."""
-    p = inputs.prefill_problem("onehot", 21, 4, 8, 64, head, 4, 1, fmt, decode_tail=8)
+    tiny blocks (MXFP4 scale near 2^-127), an overflowing variance. Windows of up to 8 rows run
+    the small-window kernels, longer ones the generic gather kernel."""
+    nrows = (1 + overlap) * ratio
+    p = inputs.prefill_problem("onehot", 21, 4, max(8, ratio), max(64, 4 * ratio), head, ratio, overlap, fmt,
+                               decode_tail=8)
     rng = np.random.default_rng(fmt)
     sw = p.state_width
     p.state[..., sw:] = -1000.0
@@ -107,11 +111,11 @@ def test_one_hot_epilogue_edges_generic(fmt, head):
         else:
             v = rng.standard_normal(head)
         pos, r = int(p.positions[t]), int(p.token_to_req[t])
-        valid = [i for i in range(8) if pos - 7 + i >= 0]
+        valid = [i for i in range(nrows) if pos - nrows + 1 + i >= 0]
         pick = rng.choice(valid, head)
         for c in range(head):
-            q = pos - 7 + pick[c]
-            ho = head if pick[c] >= 4 else 0
+            q = pos - nrows + 1 + pick[c]
+            ho = head if pick[c] >= ratio else 0
             b, o = p.block_table[r, q // 8], q % 8
             p.state[b, o, sw + ho + c] = 0.0
             p.state[b, o, ho + c] = np.float32(v[c])
@@ -124,9 +128,10 @@ def test_one_hot_epilogue_edges_generic(fmt, head):
     assert rep["e2e_bytes_differ"] == 0
 
 
-def test_padded_strides_generic():
+@pytest.mark.parametrize("name", ["idx_c4_mxfp4", "idx_c128_fp8", "c4_sparse"])
+def test_padded_strides_generic(name):
     import torch
-    p = inputs.make_next_problem("idx_c4_mxfp4")
+    p = inputs.make_next_problem(name)
     dev = to_device(p)
     NB, BS, RW = p.state.shape
     big = torch.zeros((NB, BS, RW + 36), dtype=torch.float32, device="cuda")
