@@ -411,6 +411,19 @@ def sweep(args, dev):
     return {"eager": eager, "graph": graph, "rotate4_no_flush": rot4}
 
 
+def next_algorithmic_bytes(p, pos):
+    """Bytes a window at each position in `pos` must move: the kv and score half-rows of its
+    unmasked rows (rows at negative positions are masked), one 4-byte block id per distinct state
+    block, the 64 fp32 cos/sin values and the cache slot."""
+    n = (1 + p.overlap) * p.ratio
+    rows = np.minimum(n, pos + 1)
+    first = np.maximum(pos - n + 1, 0)
+    sb = int(p.state.shape[1])
+    blocks = pos // sb - first // sb + 1
+    slot = {0: 584, 1: 132, 2: 68}[p.fmt]
+    return int((rows * 2 * p.head * 4 + blocks * 4 + 256 + slot).sum())
+
+
 def bench_next(args, dev):
     """The other configurations of the pages' fused kernels through compress_norm_rope_store_ex
     (C4 overlap with the sparse-attention cache; the head-128 indexer with FP8 or MXFP4 caches at
@@ -449,15 +462,15 @@ def bench_next(args, dev):
             b.record(stream)
             torch.cuda.synchronize()
         assert binding.device_errors(clear=True) == 0
-        A = int(((p.positions + 1) % p.ratio == 0).sum())   # every token here has a slot; window ends
-        rows = (1 + p.overlap) * p.ratio
-        tb, sb = {0: (576, 8), 1: (128, 4), 2: (64, 4)}[p.fmt]
-        per_window = rows * 2 * p.head * 4 + rows * 4 + 256 + tb + sb
+        active = (p.positions >= 0) & ((p.positions + 1) % p.ratio == 0)   # every token here has a slot
+        A = int(active.sum())
+        total_bytes = next_algorithmic_bytes(p, p.positions[active])
+        per_window = total_bytes / max(A, 1)
         kus = kt.total_ms * 1e3 / kt.launches
-        achieved = A * per_window / (kus * 1e-6) / 1e9
+        achieved = total_bytes / (kus * 1e-6) / 1e9
         res[name] = {"tokens": p.num_tokens, "windows": A, "us_per_call": round(a.elapsed_time(b) * 1e3 / n, 2),
                      "windows_per_s": A / (a.elapsed_time(b) / n * 1e-3), "kernel_us": round(kus, 2),
-                     "algorithmic_bytes_per_window": per_window, "achieved_gbs": round(achieved, 1),
+                     "algorithmic_bytes_per_window": round(per_window, 1), "achieved_gbs": round(achieved, 1),
                      "frac_of_measured_hbm": round(achieved / peak, 3)}
         del d, p, call
         torch.cuda.empty_cache()
