@@ -52,6 +52,41 @@ __device__ __noinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const vol
     if (global_timer_ns() - t0 > kWaitTimeoutNs) return false;
   }
 }
+// Non-blocking test of a phase.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred P;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 P, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, P;\n}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// The same wait, but each retry lets the hardware suspend the thread until the phase completes
+// (at most kSuspendHintNs per try), so waiting warps take no issue slots from the warps that work.
+constexpr uint32_t kSuspendHintNs = 20000;
+__device__ __forceinline__ bool mbar_try_wait_suspend(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred P;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 P, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, P;\n}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity), "r"(kSuspendHintNs)
+      : "memory");
+  return ok != 0;
+}
+__device__ __noinline__ bool mbar_wait_suspend(uint64_t* bar, uint32_t parity, const volatile int* abort_flag) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (;;) {
+    if (mbar_try_wait_suspend(bar, parity)) return true;
+    if (abort_flag != nullptr && *abort_flag) return false;
+    if (global_timer_ns() - t0 > kWaitTimeoutNs) return false;
+  }
+}
 // L2 policy of the state stream: evict-first by default (every state byte is read once).
 #ifndef C128_L2_POLICY
 #define C128_L2_POLICY 1

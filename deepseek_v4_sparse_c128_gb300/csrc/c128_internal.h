@@ -100,6 +100,7 @@ cudaError_t launch(const Params& p, const LaunchCfg& cfg, cudaStream_t stream);
 cudaError_t launch_gather(const Params& p, const LaunchCfg& cfg, cudaStream_t stream);
 bool small_window_path(const Params& p);
 cudaError_t launch_small(const Params& p, const LaunchCfg& cfg, cudaStream_t stream);
+cudaError_t prepare_small();  // function attributes of the small-window kernels
 int compress_smem_bytes();
 cudaError_t prepare_device(int device);  // one-time function attributes
 

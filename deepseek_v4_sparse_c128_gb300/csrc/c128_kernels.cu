@@ -545,6 +545,7 @@ cudaError_t prepare_device(int /*device*/) {
   if (e == cudaSuccess) e = cudaFuncSetAttribute(direct_kernel<2>, a, static_cast<int>(sizeof(DirectSmem<2>)));
   if (e == cudaSuccess) e = cudaFuncSetAttribute(direct_kernel<4>, a, static_cast<int>(sizeof(DirectSmem<4>)));
   if (e == cudaSuccess) e = cudaFuncSetAttribute(direct_kernel<8>, a, static_cast<int>(sizeof(DirectSmem<8>)));
+  if (e == cudaSuccess) e = prepare_small();
   return e;
 }
 
