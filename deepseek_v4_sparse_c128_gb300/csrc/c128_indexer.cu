@@ -1,0 +1,403 @@
+// sm_103a kernel for head-128 windows of more than 8 rows (the indexer compressor at compress
+// ratio 128, and any ratio >= 8 whose windows exceed 8 rows): a persistent CTA per SM streams one
+// window at a time through a ring of 32 KiB shared-memory stages.
+//
+//   warp 0       scheduler: claims the next window, resolves the token's request, position and
+//                cache slot and, one lane per chunk of 8 rows, the chunk's state block, checks
+//                them and writes a window descriptor (two in flight).
+//   warp 1       copier (lane 0): per stage, up to 4 tiled TMA loads (`cp.async.bulk.tensor.5d`)
+//                of 8 rows each; the box takes the kv half-row and the score half-row of every
+//                row (the older or the newer half of an overlapping window). Completion is
+//                counted in bytes on the stage's mbarrier.
+//   warps 2..9   consumers: row group g (two warps, thread i owns columns 2i, 2i+1) folds chunk g
+//                of every stage into an online softmax; after the window's last stage the four
+//                row groups' partial states are merged, in row-group order, by consumer warp 0,
+//                which runs the indexer epilogue (RMSNorm, RoPE, FP8 or MXFP4 cache store) while
+//                the other warps go on with the next window.
+//
+// Same arithmetic as the oracle's reading of _fused_kv_compress_norm_rope_insert_indexer_attn and
+// ..._indexer_mxfp4_attn on the API page of vllm.models.deepseek_v4.common.ops.fused_compress_quant_cache.
+#include <cuda.h>
+
+#include <cstddef>
+
+#include "c128_device.cuh"
+#include "c128_warp_epilogue.cuh"
+
+namespace c128 {
+namespace {
+
+constexpr int kIxHead = 128;
+constexpr int kIxChunk = 8;                                            // rows per tiled load
+constexpr int kIxStageChunks = 4;                                      // 32 rows per stage
+constexpr int kIxStages = 6;
+constexpr int kIxMaxChunks = 32;                                       // windows of up to 256 rows
+constexpr int kIxRowFloats = 2 * kIxHead;                              // kv half-row | score half-row
+constexpr int kIxChunkFloats = kIxChunk * kIxRowFloats;                // 8 KiB
+constexpr int kIxStageFloats = kIxStageChunks * kIxChunkFloats;        // 32 KiB
+constexpr int kIxConsumerWarps = 8;
+constexpr int kIxConsumerThreads = 32 * kIxConsumerWarps;
+constexpr int kIxThreads = 32 * (2 + kIxConsumerWarps);
+constexpr int kIxRowGroups = kIxStageChunks;                           // row group g takes chunk g of a stage
+constexpr int kIxDescSlots = 2;
+static_assert(kIxRowGroups * kIxHead / 2 == kIxConsumerThreads, "two columns per consumer thread");
+
+struct __align__(16) IxDesc {
+  int32_t blk[kIxMaxChunks];   // state block of each present chunk, oldest first
+  int32_t row[kIxMaxChunks];   // the chunk's first row within its block
+  int32_t half[kIxMaxChunks];  // 0: older half of an overlapping window (or no overlap), 1: newer half
+  uint8_t* tok;                // token bytes of the cache slot
+  uint8_t* scale;              // scale bytes of the slot
+  const float* cs_row;         // cos/sin row (p / ratio) * ratio
+  float* comp_dst;             // optional fp32 export
+  int32_t nchunks;             // chunks present; 0 marks the end of the work
+  int32_t pad[3];
+};
+
+struct IxSmem {
+  float stage[kIxStages][kIxStageFloats];
+  IxDesc desc[kIxDescSlots];
+  uint64_t full[kIxStages];       // stage landed (1 arrival + its bytes)
+  uint64_t empty[kIxStages];      // stage consumed (one arrival per consumer warp)
+  uint64_t dfull[kIxDescSlots];   // descriptor written (scheduler)
+  uint64_t dempty[kIxDescSlots];  // descriptor released (copier + consumer warps)
+  // row-group partial states (log2-unit max, sum, weighted sum), double-buffered by window parity
+  alignas(16) float part_m[2][kIxRowGroups][kIxHead];
+  alignas(16) float part_l[2][kIxRowGroups][kIxHead];
+  alignas(16) float part_a[2][kIxRowGroups][kIxHead];
+  alignas(16) float comp_s[kIxHead];  // exact-variance slow path of the epilogue warp (float4 stores)
+  int abort_flag;
+};
+static_assert(sizeof(IxSmem) <= 227 * 1024, "shared memory");
+static_assert(sizeof(float) * kIxStageFloats % 128 == 0 && sizeof(float) * kIxChunkFloats % 128 == 0,
+              "tiled-load destinations stay 128-byte aligned");
+
+__device__ __forceinline__ void ix_set_timeout(const Params& p, int* abort_flag) {
+  *reinterpret_cast<volatile int*>(abort_flag) = 1;
+  atomicOr(&p.ws->err, static_cast<unsigned>(C128_DEV_TIMEOUT));
+}
+
+__device__ __forceinline__ void ix_tma_load(void* dst, const CUtensorMap* map, int half, int row, int blk,
+                                            uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint "
+      "[%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(half), "r"(0), "r"(row), "r"(blk), "r"(smem_addr(bar)),
+      "l"(policy)
+      : "memory");
+}
+
+// ------------------------------------------------------------------------------ scheduler warp
+template <int FMT>
+__device__ void ix_scheduler(const Params& p, IxSmem& S, int lane) {
+  constexpr int kTok = FMT == C128_FORMAT_INDEXER_FP8 ? 128 : 64;
+  grid_dependency_wait();  // the list and the counters come from plan_kernel
+  const int32_t* list = reinterpret_cast<const int32_t*>(p.ws + 1);
+  const volatile int* abort_flag = &S.abort_flag;
+  const uint32_t A = static_cast<uint32_t>(min(static_cast<int64_t>(*reinterpret_cast<volatile unsigned*>(&p.ws->count)), p.T));
+  const int n = (1 + p.overlap) * p.ratio;  // 16..256 rows, a multiple of 8
+  uint32_t widx = 0;
+  for (;;) {
+    if (*abort_flag) return;
+    uint32_t a = 0;
+    if (lane == 0) a = atomicAdd(&p.ws->next, 1u);
+    a = __shfl_sync(0xffffffffu, a, 0);
+    const bool end = a >= A;
+    long long t = 0, pos = 0, kvs = 0;
+    int req = 0;
+    uint32_t err = 0;
+    if (!end) {
+      if (lane == 0) {
+        t = list[a];
+        req = __ldg(p.ttr + t);
+        pos = __ldg(p.pos + t);
+        kvs = __ldg(p.kvslot + t);
+        if (req < 0 || req >= p.bt_rows) err |= C128_DEV_BAD_REQ;
+        if (pos / p.sblk >= p.bt_cols) err |= C128_DEV_BAD_BT_COL;
+        if ((pos & ~static_cast<long long>(p.ratio - 1)) >= p.cs_rows) err |= C128_DEV_BAD_COS_ROW;
+        if (kvs >= p.nkb * p.kv_bs) err |= C128_DEV_BAD_KV_SLOT;
+      }
+      t = __shfl_sync(0xffffffffu, t, 0);
+      req = __shfl_sync(0xffffffffu, req, 0);
+      pos = __shfl_sync(0xffffffffu, pos, 0);
+      kvs = __shfl_sync(0xffffffffu, kvs, 0);
+      err = __shfl_sync(0xffffffffu, err, 0);
+    }
+    // window rows start .. pos; start and 0 are multiples of 8, so masked rows fill whole chunks
+    const long long start = pos - n + 1, first = start > 0 ? start : 0;
+    const int nch = end ? 0 : static_cast<int>((pos - first + 1) / kIxChunk);
+    int blk = 0, row = 0, half = 0;
+    if (!end && !(err & (C128_DEV_BAD_REQ | C128_DEV_BAD_BT_COL))) {
+      bool bad = false;
+      if (lane < nch) {
+        const long long q0 = first + static_cast<long long>(kIxChunk) * lane;
+        blk = __ldg(p.bt + static_cast<int64_t>(req) * p.bt_stride + q0 / p.sblk);
+        row = static_cast<int>(q0 % p.sblk);
+        half = (p.overlap && q0 - start >= p.ratio) ? 1 : 0;
+        bad = blk < 0 || blk >= p.nb;
+      }
+      if (__any_sync(0xffffffffu, bad)) err |= C128_DEV_BAD_BLOCK;
+    }
+    if (!end && err) {
+      if (lane == 0) atomicOr(&p.ws->err, err);
+      continue;
+    }
+    const int ds = widx % kIxDescSlots;
+    if (widx >= kIxDescSlots) {
+      bool ok = mbar_wait_suspend(&S.dempty[ds], ((widx / kIxDescSlots) - 1u) & 1u, abort_flag);
+      if (!__all_sync(0xffffffffu, ok)) {
+        if (lane == 0) ix_set_timeout(p, &S.abort_flag);
+        return;
+      }
+    }
+    IxDesc& d = S.desc[ds];
+    if (lane < nch) {
+      d.blk[lane] = blk;
+      d.row[lane] = row;
+      d.half[lane] = half;
+    }
+    if (lane == 0) {
+      if (!end) {
+        const long long kb = kvs / p.kv_bs, off = kvs - kb * p.kv_bs;
+        uint8_t* base = p.kc + kb * p.kc_stride0;
+        d.tok = base + off * kTok;
+        d.scale = base + p.kv_bs * kTok + off * 4;
+        d.cs_row = p.cs + (pos & ~static_cast<long long>(p.ratio - 1)) * p.cs_stride;
+        d.comp_dst = p.comp_out ? p.comp_out + t * kIxHead : nullptr;
+      }
+      d.nchunks = nch;
+    }
+    __syncwarp();
+    if (lane == 0) {
+      __threadfence_block();
+      mbar_arrive(&S.dfull[ds]);
+    }
+    ++widx;
+    if (end) return;
+  }
+}
+
+// --------------------------------------------------------------------------------- copier thread
+__device__ void ix_copier(const Params& p, IxSmem& S, const CUtensorMap* map) {
+  const volatile int* abort_flag = &S.abort_flag;
+  const uint64_t policy = l2_evict_first_policy();
+  uint32_t it = 0, widx = 0;
+  bool failed = false;
+  for (;;) {
+    const int ds = widx % kIxDescSlots;
+    if (!mbar_wait_suspend(&S.dfull[ds], (widx / kIxDescSlots) & 1u, abort_flag)) {
+      failed = true;
+      break;
+    }
+    const IxDesc& d = S.desc[ds];
+    const int nch = d.nchunks;
+    if (nch == 0) break;
+    for (int c0 = 0; c0 < nch; c0 += kIxStageChunks) {
+      const int s = it % kIxStages;
+      const uint32_t round = it / kIxStages;
+      if (round > 0 && !mbar_wait_suspend(&S.empty[s], (round - 1u) & 1u, abort_flag)) {
+        failed = true;
+        break;
+      }
+      const int cnt = min(kIxStageChunks, nch - c0);
+      mbar_arrive_expect_tx(&S.full[s], static_cast<uint32_t>(cnt * kIxChunkFloats * 4));
+      for (int j = 0; j < cnt; ++j)
+        ix_tma_load(S.stage[s] + j * kIxChunkFloats, map, d.half[c0 + j], d.row[c0 + j], d.blk[c0 + j], &S.full[s],
+                    policy);
+      ++it;
+    }
+    if (failed) break;
+    mbar_arrive(&S.dempty[ds]);
+    ++widx;
+  }
+  if (failed) {
+    ix_set_timeout(p, &S.abort_flag);
+    // let every copy this thread issued land before the CTA may exit
+    for (uint32_t i = it > static_cast<uint32_t>(kIxStages) ? it - kIxStages : 0u; i < it; ++i)
+      mbar_wait(&S.full[i % kIxStages], (i / kIxStages) & 1u, nullptr);
+  }
+}
+
+// ------------------------------------------------------------------------------ consumer warps
+// Fold the 8 rows of one staged chunk into the online state of columns c0, c0 + 1.
+__device__ __forceinline__ void ix_fold_chunk(const float* st, int c0, Online& o) {
+  float2 kv[kIxChunk], sc[kIxChunk];
+#pragma unroll
+  for (int r = 0; r < kIxChunk; ++r) {
+    kv[r] = *reinterpret_cast<const float2*>(st + r * kIxRowFloats + c0);
+    sc[r] = *reinterpret_cast<const float2*>(st + r * kIxRowFloats + kIxHead + c0);
+  }
+  float mx0 = sc[0].x, mx1 = sc[0].y;
+#pragma unroll
+  for (int r = 1; r < kIxChunk; ++r) {
+    mx0 = fmaxf(mx0, sc[r].x);
+    mx1 = fmaxf(mx1, sc[r].y);
+  }
+  const float n0 = fmaxf(o.m0, mx0 * kLog2e), n1 = fmaxf(o.m1, mx1 * kLog2e);
+  const float b0 = n0 == -INFINITY ? 0.f : n0, b1 = n1 == -INFINITY ? 0.f : n1;
+  const float r0 = ex2_approx(o.m0 - b0), r1 = ex2_approx(o.m1 - b1);
+  o.m0 = n0;
+  o.m1 = n1;
+  float ps0 = 0.f, ps1 = 0.f, pk0 = 0.f, pk1 = 0.f;
+#pragma unroll
+  for (int r = 0; r < kIxChunk; ++r) {
+    const float e0 = ex2_approx(fmaf(sc[r].x, kLog2e, -b0));
+    const float e1 = ex2_approx(fmaf(sc[r].y, kLog2e, -b1));
+    ps0 += e0;
+    ps1 += e1;
+    pk0 = fmaf(e0, kv[r].x, pk0);
+    pk1 = fmaf(e1, kv[r].y, pk1);
+  }
+  o.l0 = fmaf(o.l0, r0, ps0);
+  o.l1 = fmaf(o.l1, r1, ps1);
+  o.a0 = fmaf(o.a0, r0, pk0);
+  o.a1 = fmaf(o.a1, r1, pk1);
+}
+
+template <int FMT>
+__device__ void ix_consumers(const Params& p, IxSmem& S, int ci) {
+  const int cw = ci >> 5, lane = ci & 31;
+  const int rg = ci / (kIxHead / 2);     // row group: chunk rg of every stage
+  const int c0 = 2 * (ci % (kIxHead / 2));
+  const volatile int* abort_flag = &S.abort_flag;
+  // the epilogue warp (consumer warp 0): lane l owns columns 4l..4l+3
+  const float2 wa = *reinterpret_cast<const float2*>(p.rms_w + 4 * lane);
+  const float2 wb = *reinterpret_cast<const float2*>(p.rms_w + 4 * lane + 2);
+  uint32_t it = 0, widx = 0;
+  for (;;) {
+    const int ds = widx % kIxDescSlots;
+    const bool got = mbar_wait_suspend(&S.dfull[ds], (widx / kIxDescSlots) & 1u, abort_flag);
+    int nch = 0;
+    uint8_t* tok = nullptr;
+    uint8_t* scale = nullptr;
+    const float* cs_row = nullptr;
+    float* comp_dst = nullptr;
+    if (got) {
+      const IxDesc& d = S.desc[ds];
+      nch = d.nchunks;
+      tok = d.tok;
+      scale = d.scale;
+      cs_row = d.cs_row;
+      comp_dst = d.comp_dst;
+    } else {
+      ix_set_timeout(p, &S.abort_flag);
+    }
+    if (consumer_bar_or(!got || nch == 0 || *abort_flag)) return;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&S.dempty[ds]);  // the fields above are in registers
+
+    float2 cosv = make_float2(1.f, 1.f), sinv = make_float2(0.f, 0.f);
+    if (cw == 0 && lane >= 16) {  // pairs 2l, 2l + 1 >= 32 rotate
+      const int j0 = 2 * lane - 32;
+      cosv = make_float2(__ldg(cs_row + j0), __ldg(cs_row + j0 + 1));
+      sinv = make_float2(__ldg(cs_row + kRope / 2 + j0), __ldg(cs_row + kRope / 2 + j0 + 1));
+    }
+    Online o;
+    online_init(o);
+    bool failed = false;
+    for (int cs0 = 0; cs0 < nch; cs0 += kIxStageChunks) {
+      const int s = it % kIxStages;
+      bool ok = !failed && mbar_wait_suspend(&S.full[s], (it / kIxStages) & 1u, abort_flag);
+      ok = __all_sync(0xffffffffu, ok);
+      if (ok) {
+        if (cs0 + rg < nch) ix_fold_chunk(S.stage[s] + rg * kIxChunkFloats, c0, o);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&S.empty[s]);
+      } else {
+        failed = true;
+      }
+      ++it;
+    }
+    if (failed) ix_set_timeout(p, &S.abort_flag);
+    const int pb = widx & 1;
+    *reinterpret_cast<float2*>(&S.part_m[pb][rg][c0]) = make_float2(o.m0, o.m1);
+    *reinterpret_cast<float2*>(&S.part_l[pb][rg][c0]) = make_float2(o.l0, o.l1);
+    *reinterpret_cast<float2*>(&S.part_a[pb][rg][c0]) = make_float2(o.a0, o.a1);
+    if (consumer_bar_or(failed)) return;  // partials written; every consumer agrees on the outcome
+    if (cw == 0) {
+      // merge the row groups in order, columns 4l..4l+3
+      float out[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int col = 4 * lane + j;
+        float M = S.part_m[pb][0][col];
+#pragma unroll
+        for (int g = 1; g < kIxRowGroups; ++g) M = fmaxf(M, S.part_m[pb][g][col]);
+        const float B = M == -INFINITY ? 0.f : M;
+        float L = 0.f, Acc = 0.f;
+#pragma unroll
+        for (int g = 0; g < kIxRowGroups; ++g) {
+          const float sc = ex2_approx(S.part_m[pb][g][col] - B);
+          L = fmaf(S.part_l[pb][g][col], sc, L);
+          Acc = fmaf(S.part_a[pb][g][col], sc, Acc);
+        }
+        out[j] = __fdiv_rn(Acc, L);
+      }
+      indexer_warp_epilogue<FMT>(make_float4(out[0], out[1], out[2], out[3]), lane, wa, wb, p.eps, cosv, sinv, tok,
+                                 scale, comp_dst, S.comp_s);
+    }
+    ++widx;
+  }
+}
+
+template <int FMT>
+__global__ void __launch_bounds__(kIxThreads, 1)
+    indexer_window_kernel(Params p, const __grid_constant__ CUtensorMap state_map) {
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  IxSmem& S = *reinterpret_cast<IxSmem*>(smem_raw);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid == 0) {
+    for (int s = 0; s < kIxStages; ++s) {
+      mbar_init(&S.full[s], 1);
+      mbar_init(&S.empty[s], kIxConsumerWarps);
+    }
+    for (int d = 0; d < kIxDescSlots; ++d) {
+      mbar_init(&S.dfull[d], 1);
+      mbar_init(&S.dempty[d], kIxConsumerWarps + 1);
+    }
+    S.abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  if (warp == 0) {
+    ix_scheduler<FMT>(p, S, lane);
+  } else if (warp == 1) {
+    if (lane == 0) ix_copier(p, S, &state_map);
+  } else {
+    ix_consumers<FMT>(p, S, tid - 64);
+  }
+}
+
+}  // namespace
+
+cudaError_t prepare_indexer_windows() {
+  const cudaFuncAttribute a = cudaFuncAttributeMaxDynamicSharedMemorySize;
+  cudaError_t e = cudaFuncSetAttribute(indexer_window_kernel<C128_FORMAT_INDEXER_FP8>, a, static_cast<int>(sizeof(IxSmem)));
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(indexer_window_kernel<C128_FORMAT_INDEXER_MXFP4>, a, static_cast<int>(sizeof(IxSmem)));
+  return e;
+}
+
+cudaError_t launch_indexer_windows(const Params& p, const LaunchCfg& cfg, cudaStream_t stream) {
+  const int n = (1 + p.overlap) * p.ratio;
+  if (p.head != kIxHead || p.fmt == C128_FORMAT_SPARSE_FP8 || n <= 8 || n > kIxChunk * kIxMaxChunks ||
+      p.ratio % kIxChunk != 0)
+    return cudaErrorNotSupported;
+  CUtensorMap map;
+  if (!encode_state_map(p, kIxHead, kIxChunk, &map)) return cudaErrorNotSupported;
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = dim3(static_cast<unsigned>(cfg.sm_count));  // one persistent CTA per SM
+  lc.blockDim = dim3(kIxThreads);
+  lc.dynamicSmemBytes = sizeof(IxSmem);
+  lc.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  lc.attrs = attr;
+  lc.numAttrs = (cfg.pdl && cfg.ev_begin == nullptr) ? 1 : 0;
+  if (p.fmt == C128_FORMAT_INDEXER_FP8)
+    return cudaLaunchKernelEx(&lc, indexer_window_kernel<C128_FORMAT_INDEXER_FP8>, p, map);
+  return cudaLaunchKernelEx(&lc, indexer_window_kernel<C128_FORMAT_INDEXER_MXFP4>, p, map);
+}
+
+}  // namespace c128

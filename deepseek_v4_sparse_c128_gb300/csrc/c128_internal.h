@@ -1,5 +1,6 @@
 // Internal declarations shared by the kernel translation unit and the C-ABI layer.
 #pragma once
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -101,6 +102,13 @@ cudaError_t launch_gather(const Params& p, const LaunchCfg& cfg, cudaStream_t st
 bool small_window_path(const Params& p);
 cudaError_t launch_small(const Params& p, const LaunchCfg& cfg, cudaStream_t stream);
 cudaError_t prepare_small();  // function attributes of the small-window kernels
+// Head-128 windows of more than 8 rows (c128_indexer.cu); cudaErrorNotSupported (nothing
+// launched) when the configuration or the state layout does not fit that kernel.
+cudaError_t launch_indexer_windows(const Params& p, const LaunchCfg& cfg, cudaStream_t stream);
+cudaError_t prepare_indexer_windows();
+// Tensor map of the state cache for tiled loads of `box_rows` rows x (head kv + head score
+// columns); false when the layout does not allow one (c128_c4.cu).
+bool encode_state_map(const Params& p, int head, int box_rows, CUtensorMap* map);
 int compress_smem_bytes();
 cudaError_t prepare_device(int device);  // one-time function attributes
 

@@ -546,6 +546,7 @@ cudaError_t prepare_device(int /*device*/) {
   if (e == cudaSuccess) e = cudaFuncSetAttribute(direct_kernel<4>, a, static_cast<int>(sizeof(DirectSmem<4>)));
   if (e == cudaSuccess) e = cudaFuncSetAttribute(direct_kernel<8>, a, static_cast<int>(sizeof(DirectSmem<8>)));
   if (e == cudaSuccess) e = prepare_small();
+  if (e == cudaSuccess) e = prepare_indexer_windows();
   return e;
 }
 
@@ -557,7 +558,12 @@ cudaError_t launch(const Params& p, const LaunchCfg& cfg, cudaStream_t stream) {
     plan_kernel<<<plan_grid, kPlanThreads, 0, stream>>>(p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (cfg.ev_begin != nullptr && (e = cudaEventRecord(cfg.ev_begin, stream)) != cudaSuccess) return e;
-    e = small_window_path(p) ? launch_small(p, cfg, stream) : launch_gather(p, cfg, stream);
+    if (small_window_path(p)) {
+      e = launch_small(p, cfg, stream);
+    } else {
+      e = launch_indexer_windows(p, cfg, stream);
+      if (e == cudaErrorNotSupported) e = launch_gather(p, cfg, stream);
+    }
     if (e != cudaSuccess) return e;
     if (cfg.ev_end != nullptr) e = cudaEventRecord(cfg.ev_end, stream);
     return e;

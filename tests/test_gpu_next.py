@@ -41,6 +41,19 @@ def test_other_state_block_sizes(block, fmt, head):
     check_against_oracle_ex(p, kc, comp, threads=16)
 
 
+@pytest.mark.parametrize("block", [1, 4, 8, 16, 64])
+@pytest.mark.parametrize("fmt,ratio,overlap", [(1, 16, 1), (2, 128, 0), (1, 8, 1)])
+def test_indexer_long_windows_block_sizes(block, fmt, ratio, overlap):
+    """Head-128 windows longer than 8 rows: state blocks that are multiples of 8 rows take the
+    tiled-load ring kernel, the others the gather kernel; both against the oracle."""
+    p = inputs.prefill_problem("ixblk", 31 + block, 5, 5, 40 * ratio, 128, ratio, overlap, fmt, state_block=block,
+                               kv_block_size=16, decode_tail=6)
+    kc, comp, err = run_gpu_ex(p)
+    assert err == 0
+    rep = check_against_oracle_ex(p, kc, comp, threads=16)
+    assert rep["stored"] > 10
+
+
 def test_c128_config_through_ex_is_the_c128_call():
     for name in ("decode", "mixed"):
         p = inputs.make_problem(name)
@@ -59,7 +72,7 @@ def test_c128_config_with_other_block_size_uses_generic_path():
     check_against_oracle_ex(p, kc, comp, threads=16)
 
 
-@pytest.mark.parametrize("name", ["idx_c4_fp8", "c4_sparse"])
+@pytest.mark.parametrize("name", ["idx_c4_fp8", "c4_sparse", "idx_c128_mxfp4"])
 def test_bad_indices_generic_path(name):
     p = inputs.make_next_problem(name)
     act = [t for t in range(p.num_tokens) if p.kv_slot_mapping[t] >= 0 and p.positions[t] >= 7]
@@ -69,7 +82,7 @@ def test_bad_indices_generic_path(name):
     q = int(p.positions[t_blk]) - 2
     p.block_table[r, q // p.state.shape[1]] = p.state.shape[0]
     p.kv_slot_mapping[t_kv] = p.k_cache.shape[0] * p.kv_block_size
-    p.positions[t_bt] = p.block_table.shape[1] * p.state.shape[1] + 3
+    p.positions[t_bt] = p.block_table.shape[1] * p.state.shape[1] + p.ratio - 1  # a window end past the table
     kc, comp, err = run_gpu_ex(p)
     ref = p.k_cache.copy()
     err_ref = oracle.forward_ex(p, k_cache=ref)
@@ -85,7 +98,8 @@ def test_one_hot_epilogue_edges_generic(fmt, head, ratio, overlap):
     """One-hot scores (0 on one valid row, -1000 elsewhere) make comp32 equal crafted kv values on
     both sides: wide dynamic range (slow exact variance), subnormals, zeros, E2M1/e4m3 ties,
     tiny blocks (MXFP4 scale near 2^-127), an overflowing variance. Windows of up to 8 rows run
-    the small-window kernels, longer ones the generic gather kernel."""
+    the small-window kernel, longer head-128 windows the tiled-load ring kernel, longer head-512
+    windows the gather kernel."""
     nrows = (1 + overlap) * ratio
     p = inputs.prefill_problem("onehot", 21, 4, max(8, ratio), max(64, 4 * ratio), head, ratio, overlap, fmt,
                                decode_tail=8)
