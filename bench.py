@@ -39,7 +39,7 @@ HEADLINE_T = 16374
 STATE_BYTES_PER_WINDOW = 128 * 1024 * 4                       # 524,288
 ALGO_BYTES_PER_WINDOW = STATE_BYTES_PER_WINDOW + 64 + 256 + 584  # + block ids, cos/sin row, k_cache write
 PAGES_US_16374 = 1425.900  # vLLM PR #44230, Performance table (B300), token_num 16374
-KERNEL_SRC = os.path.join(ROOT, "deepseek_v4_sparse_c128_gb300", "csrc", "c128_kernels.cu")
+OTHER_TRAFFIC_FILE = os.path.join(ROOT, "profiles", "other_configurations_traffic.json")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "compress_kernel_sweep1024_traffic.json")
 
 
@@ -334,17 +334,30 @@ def run_ours(args, ws, rank, local):
         print(json.dumps(out), flush=True)
 
 
+def sources_sha256(files) -> str:
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def current_traffic_record(rec):
+    """The record if the kernel sources it lists are unchanged since its ncu capture, else None."""
+    try:
+        return rec if rec.get("kernel_source_sha256") == sources_sha256(rec["kernel_sources"]) else None
+    except (OSError, KeyError, TypeError):
+        return None
+
+
 def traffic_per_launch(T: int):
     """DRAM bytes per launch from the committed ncu capture, scaled by windows, or None when the
-    kernel source changed since the capture."""
+    kernel's sources changed since the capture."""
     try:
-        rec = json.load(open(TRAFFIC_FILE))
+        rec = current_traffic_record(json.load(open(TRAFFIC_FILE)))
     except (OSError, ValueError):
         return None
-    src_hash = hashlib.sha256(open(KERNEL_SRC, "rb").read()).hexdigest()
-    if rec.get("kernel_source_sha256") != src_hash:
-        return None
-    return rec["dram_bytes_per_window"] * T
+    return None if rec is None else rec["dram_bytes_per_window"] * T
 
 
 def sweep(args, dev):
@@ -437,9 +450,12 @@ def bench_next(args, dev):
     except (OSError, ValueError):
         pass
     peak = float(peaks.get("hbm_gbs", 6800.0))
+    try:
+        traffic = json.load(open(OTHER_TRAFFIC_FILE))
+    except (OSError, ValueError):
+        traffic = {}
     res = {}
-    for name, scale in (("c4_sparse", 64), ("idx_c4_fp8", 64), ("idx_c4_mxfp4", 64), ("idx_c128_fp8", 16),
-                        ("idx_c128_mxfp4", 16)):
+    for name, scale in NEXT_SCALES.items():
         p = inputs.make_next_problem(name, state_device=str(dev), scale=scale)
         to = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
         d = {k: to(getattr(p, k)) for k in ("token_to_req", "positions", "slot_mapping", "block_table", "rms_w",
@@ -472,6 +488,8 @@ def bench_next(args, dev):
                      "windows_per_s": A / (a.elapsed_time(b) / n * 1e-3), "kernel_us": round(kus, 2),
                      "algorithmic_bytes_per_window": round(per_window, 1), "achieved_gbs": round(achieved, 1),
                      "frac_of_measured_hbm": round(achieved / peak, 3)}
+        rec = current_traffic_record(traffic.get(name)) if isinstance(traffic.get(name), dict) else None
+        res[name]["ncu_dram_bytes_per_window"] = None if rec is None else rec["dram_bytes_per_window"]
         del d, p, call
         torch.cuda.empty_cache()
     return res
@@ -511,6 +529,48 @@ def run_reference(args, ws, rank):
     print(json.dumps(out), flush=True)
 
 
+NEXT_SCALES = {"c4_sparse": 64, "idx_c4_fp8": 64, "idx_c4_mxfp4": 64, "idx_c128_fp8": 16, "idx_c128_mxfp4": 16}
+
+
+def run_case(args):
+    """One workload alone, `--warmup` + `--steps` calls on one stream with nothing else around
+    them (the command the ncu summaries under profiles/ are taken with): `sweep` (the headline
+    layout at --tokens) or one of the other configurations at its bench size."""
+    import torch
+    from deepseek_v4_sparse_c128_gb300 import binding, build
+    build.build()
+    binding.load()
+    dev = torch.device("cuda", 0)
+    if args.case == "sweep":
+        p = inputs.make_problem("sweep", tokens=args.tokens, state_device=str(dev))
+        cfg = None
+    else:
+        p = inputs.make_next_problem(args.case, state_device=str(dev), scale=NEXT_SCALES[args.case])
+        cfg = binding.config(p.head, p.ratio, p.overlap, p.state_width, p.fmt)
+    to = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    d = {k: to(getattr(p, k)) for k in ("token_to_req", "positions", "slot_mapping", "block_table", "rms_w",
+                                        "cos_sin", "k_cache", "kv_slot_mapping")}
+    stream = torch.cuda.current_stream()
+    call = binding.PreparedCall(d["token_to_req"], d["positions"], d["slot_mapping"], d["block_table"], p.state,
+                                d["rms_w"], p.eps, d["cos_sin"], d["k_cache"], d["kv_slot_mapping"], p.kv_block_size,
+                                stream=stream, cfg=cfg)
+    binding.reserve_workspace(p.num_tokens)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for _ in range(args.warmup):
+        call()
+    a.record(stream)
+    for _ in range(args.steps):
+        call()
+    b.record(stream)
+    torch.cuda.synchronize()
+    errs = binding.device_errors(clear=True)
+    print(json.dumps({"case": args.case, "tokens": p.num_tokens, "calls": args.steps,
+                      "us_per_call": a.elapsed_time(b) * 1e3 / max(args.steps, 1), "device_errors": errs}), flush=True)
+    if errs:
+        raise SystemExit(1)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -522,7 +582,12 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-next", action="store_true")
+    ap.add_argument("--case", choices=["sweep"] + list(NEXT_SCALES),
+                    help="run one workload alone (no JSON bench line); used for profiling")
     args = ap.parse_args()
+    if args.case:
+        run_case(args)
+        return
     ws, rank, local = dist_setup()
     try:
         if args.impl == "reference":
