@@ -34,6 +34,8 @@ constexpr int kThreads = 64 + 32 * kConsumerWarps;  // scheduler warp, copy warp
 constexpr int kPlanThreads = 256;
 constexpr int kPlanTokensPerThread = 8;
 constexpr int kPlanTokensPerCta = kPlanThreads * kPlanTokensPerThread;
+// Up to this many tokens per SM the C128 kernel runs without the planning pass (token striding).
+constexpr int kStridedTokensPerSm = 8;
 constexpr unsigned long long kWaitTimeoutNs = 1000ull * 1000ull * 1000ull;  // 1 s per wait
 
 // Workspace layout: a 256-byte header then the list of active token indices.
@@ -70,6 +72,7 @@ struct Params {
   int32_t sw;                 // state width: kv columns of a row, as many score columns follow
   int32_t fmt;                // cache format (C128_FORMAT_*)
   int64_t sblk;               // state-cache block size (rows per block)
+  int32_t strided;            // C128 kernel only: no planning pass, CTA c takes tokens c, c + grid, ...
 };
 
 // True for the configuration the specialised C128 kernels serve.

@@ -89,23 +89,49 @@ struct Smem {
 };
 
 __device__ void scheduler_warp(const Params& p, Smem& S, int lane) {
-  grid_dependency_wait();  // the list and the counters come from plan_kernel
+  const bool strided = p.strided != 0;
+  if (!strided) grid_dependency_wait();  // the list and the counters come from plan_kernel
   const int32_t* list = reinterpret_cast<const int32_t*>(p.ws + 1);
   const volatile int* abort_flag = &S.abort_flag;
-  const uint32_t A = static_cast<uint32_t>(min(static_cast<int64_t>(*reinterpret_cast<volatile unsigned*>(&p.ws->count)), p.T));
+  const uint32_t A =
+      strided ? 0u : static_cast<uint32_t>(min(static_cast<int64_t>(*reinterpret_cast<volatile unsigned*>(&p.ws->count)), p.T));
+  int64_t next_t = blockIdx.x;  // token striding: this CTA's next candidate token
   uint32_t widx = 0;
   for (;;) {
     if (*abort_flag) return;
-    uint32_t a = 0;
-    if (lane == 0) a = atomicAdd(&p.ws->next, 1u);
-    a = __shfl_sync(0xffffffffu, a, 0);
-    const bool end = a >= A;
+    bool end;
     long long t = 0, pos = 0, kvs = 0;
     int req = 0;
     uint32_t err = 0;
+    if (strided) {
+      // the next active token among next_t, next_t + grid, ...: 32 candidates per step
+      long long found = -1;
+      while (found < 0 && next_t < p.T) {
+        const int64_t c = next_t + static_cast<int64_t>(lane) * gridDim.x;
+        bool act = false;
+        if (c < p.T) {
+          const int64_t s = __ldg(p.slot + c), ps = __ldg(p.pos + c), kv = __ldg(p.kvslot + c);
+          act = (s >= 0) & (ps >= 0) & (((ps + 1) & (kRatio - 1)) == 0) & (kv >= 0);
+        }
+        const uint32_t m = __ballot_sync(0xffffffffu, act);
+        if (m) {
+          found = next_t + static_cast<int64_t>(__ffs(m) - 1) * gridDim.x;
+          next_t = found + gridDim.x;
+        } else {
+          next_t += 32ll * gridDim.x;
+        }
+      }
+      end = found < 0;
+      if (!end && lane == 0) t = found;
+    } else {
+      uint32_t a = 0;
+      if (lane == 0) a = atomicAdd(&p.ws->next, 1u);
+      a = __shfl_sync(0xffffffffu, a, 0);
+      end = a >= A;
+      if (!end && lane == 0) t = list[a];
+    }
     if (!end) {
       if (lane == 0) {
-        t = list[a];
         req = __ldg(p.ttr + t);
         pos = __ldg(p.pos + t);
         kvs = __ldg(p.kvslot + t);
@@ -575,7 +601,18 @@ cudaError_t launch(const Params& p, const LaunchCfg& cfg, cudaStream_t stream) {
     case 1: return launch_direct<1>(p, cfg, stream);
     default: break;
   }
-  cudaError_t e = cudaMemsetAsync(p.ws, 0, 2 * sizeof(unsigned int), stream);  // count, next
+  cudaError_t e;
+  if (p.T <= static_cast<int64_t>(kStridedTokensPerSm) * cfg.sm_count) {
+    // few tokens per SM: no planning pass, no counters; CTA c takes tokens c, c + grid, ...
+    Params q = p;
+    q.strided = 1;
+    if (cfg.ev_begin != nullptr && (e = cudaEventRecord(cfg.ev_begin, stream)) != cudaSuccess) return e;
+    compress_kernel<<<cfg.grid, kThreads, sizeof(Smem), stream>>>(q);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (cfg.ev_end != nullptr) e = cudaEventRecord(cfg.ev_end, stream);
+    return e;
+  }
+  e = cudaMemsetAsync(p.ws, 0, 2 * sizeof(unsigned int), stream);  // count, next
   if (e != cudaSuccess) return e;
   const int plan_grid = static_cast<int>((p.T + kPlanTokensPerCta - 1) / kPlanTokensPerCta);
   plan_kernel<<<plan_grid, kPlanThreads, 0, stream>>>(p);
