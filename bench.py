@@ -40,7 +40,7 @@ STATE_BYTES_PER_WINDOW = 128 * 1024 * 4                       # 524,288
 ALGO_BYTES_PER_WINDOW = STATE_BYTES_PER_WINDOW + 64 + 256 + 584  # + block ids, cos/sin row, k_cache write
 PAGES_US_16374 = 1425.900  # vLLM PR #44230, Performance table (B300), token_num 16374
 OTHER_TRAFFIC_FILE = os.path.join(ROOT, "profiles", "other_configurations_traffic.json")
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "compress_kernel_sweep1024_traffic.json")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "compress_kernel_sweep4096_traffic.json")
 
 
 def workload_config(T: int, n_gpus: int) -> dict:
