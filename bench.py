@@ -215,14 +215,22 @@ def run_ours(args, ws, rank, local):
     with ClockSampler(uuid) as clocks:
         barrier(ws)
         torch.cuda.synchronize()
+        # ten equal chunks of the timed steps, each between two events on the stream, for min/median
+        chunk = args.steps // 10 if args.steps >= 10 else args.steps
+        marks = []
         with binding.KernelTimer() as ktimer:
             e0.record(stream)
-            for _ in range(args.steps):
+            for i in range(args.steps):
+                if i % chunk == 0 and len(marks) < args.steps // chunk:
+                    marks.append((i, torch.cuda.Event(enable_timing=True)))
+                    marks[-1][1].record(stream)
                 step()
             e1.record(stream)
             torch.cuda.synchronize()
         barrier(ws)
     local_ms = e0.elapsed_time(e1)
+    ends = marks[1:] + [(args.steps, e1)]
+    chunk_ms = [a.elapsed_time(b) / (j - i) for (i, a), (j, b) in zip(marks, ends)]
     assert binding.device_errors(clear=True) == 0, "device error in the timed region"
     max_ms, total_windows = reduce_max_sum(ws, local_ms, float(T * args.steps))
     value = total_windows / (max_ms / 1e3)
@@ -299,8 +307,10 @@ def run_ours(args, ws, rank, local):
            "dtype": "f32", "data": "synthetic (seeded: kv~N(0,1), score~N(0,2), rms_w=1+0.1N(0,1))",
            "config": workload_config(T, ws),
            "us_per_call": ms_per_step * 1e3,
+           "us_per_call_chunks": {"chunks": len(chunk_ms), "min": min(chunk_ms) * 1e3,
+                                  "median": statistics.median(chunk_ms) * 1e3, "max": max(chunk_ms) * 1e3},
            "hbm_gbs_per_gpu": T * ALGO_BYTES_PER_WINDOW / (ms_per_step * 1e-3) / 1e9,
-           "gpu_launches": 2 * args.steps}
+           "gpu_launches": launches_per_call(T, torch.cuda.get_device_properties(dev).multi_processor_count) * args.steps}
     out["e2e"] = e2e
     peaks = {}
     try:
@@ -334,6 +344,12 @@ def run_ours(args, ws, rank, local):
         print(json.dumps(out), flush=True)
 
 
+def launches_per_call(T: int, sm_count: int) -> int:
+    """Kernels one C128 call launches: the cluster-split kernel for T x S <= #SM (S >= 1), the
+    token-striding kernel up to 8 tokens per SM, else the planning kernel and the compress kernel."""
+    return 1 if T <= 8 * sm_count else 2
+
+
 def sources_sha256(files) -> str:
     h = hashlib.sha256()
     for f in files:
@@ -364,11 +380,13 @@ def sweep(args, dev):
     """µs per call vs token_num. Before every timed call a 512 MB buffer is written (L2 flush); the
     flush, the events and the call are enqueued back to back and synchronised once per size, so
     host launch time hides behind the flush. Columns: eager calls, CUDA-graph replays of the same
-    call, and the pages' method (four input sets in rotation, back to back, no flush)."""
+    call, the pages' method (four input sets in rotation, back to back, no flush), and a cold
+    rotation (enough state sets that four times L2 separates two uses of one set, no flush)."""
     import torch
     from deepseek_v4_sparse_c128_gb300 import binding
     flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
-    eager, graph, rot4 = {}, {}, {}
+    l2 = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 129 * 1024 * 1024))
+    eager, graph, rot4, cold = {}, {}, {}, {}
     for T in inputs.SWEEP_TOKENS:
         p = inputs.make_problem("sweep", tokens=T, state_device=str(dev))
         to = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
@@ -407,6 +425,27 @@ def sweep(args, dev):
             s.synchronize()
             rot4[str(T)] = round(a.elapsed_time(b) * 1e3 / (4 * n), 3)
             del sets
+            # cold rotation: R = max(4, ceil(4 L2 / state bytes per call)) state sets cycled, no flush,
+            # so every call reads state that is not in L2 and nothing dirty is left to write back
+            nb = p.state.shape[0]
+            R = max(4, min(1024, -(-4 * l2 // (nb * p.state.shape[1] * p.state.shape[2] * 4))))
+            if R == 4:
+                cold[str(T)] = rot4[str(T)]
+            else:
+                big = inputs.draw_state(3000 + T, R * nb, str(dev))
+                sets = [binding.PreparedCall(d["token_to_req"], d["positions"], d["slot_mapping"], d["block_table"],
+                                             big[k * nb:(k + 1) * nb], d["rms_w"], p.eps, d["cos_sin"], d["k_cache"],
+                                             d["kv_slot_mapping"], p.kv_block_size, stream=s) for k in range(R)]
+                for c in sets:
+                    c()
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(s)
+                for i in range(4 * n):
+                    sets[i % R]()
+                b.record(s)
+                s.synchronize()
+                cold[str(T)] = round(a.elapsed_time(b) * 1e3 / (4 * n), 3)
+                del sets, big
             for mode, fn in (("eager", call), ("graph", g.replay)):
                 evs = []
                 for _ in range(n):
@@ -421,7 +460,7 @@ def sweep(args, dev):
                 (eager if mode == "eager" else graph)[str(T)] = round(us, 3)
             assert binding.device_errors(s, clear=True) == 0
         del d, p, g, call
-    return {"eager": eager, "graph": graph, "rotate4_no_flush": rot4}
+    return {"eager": eager, "graph": graph, "rotate4_no_flush": rot4, "rotate_cold_no_flush": cold}
 
 
 def next_algorithmic_bytes(p, pos):
