@@ -28,6 +28,7 @@ EXPORTS = (
     "c128_compress_norm_rope_store_debug",
     "c128_compress_norm_rope_store_noalloc",
     "compress_norm_rope_store_ex",
+    "c128_debug_stall_first_window",
     "c128_status_string",
     "c128_reserve_workspace",
     "c128_device_errors",
@@ -91,6 +92,7 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     L.compress_norm_rope_store.argtypes = [T, T, T, T, T, T, ctypes.c_float, T, T, T, i64, vp]
     L.c128_compress_norm_rope_store_debug.argtypes = [T, T, T, T, T, T, ctypes.c_float, T, T, T, i64, T, vp]
     L.c128_compress_norm_rope_store_noalloc.argtypes = [T, T, T, T, T, T, ctypes.c_float, T, T, T, i64, vp]
+    L.c128_debug_stall_first_window.argtypes = [T, T, T, T, T, T, ctypes.c_float, T, T, T, i64, vp]
     L.compress_norm_rope_store_ex.argtypes = [ctypes.POINTER(Config), T, T, T, T, T, T, ctypes.c_float, T, T, T, i64,
                                               T, vp]
     L.c128_status_string.argtypes = [ctypes.c_int]
@@ -188,6 +190,21 @@ def compress_norm_rope_store_ex(cfg: Config, token_to_req_indices, positions, sl
                                        ctypes.byref(cs), ctypes.byref(kc), ctypes.byref(kvs), int(kv_block_size),
                                        ctypes.byref(co) if co is not None else None, _stream_handle(stream))
     _check(rc, "compress_norm_rope_store_ex")
+
+
+def debug_stall_first_window(token_to_req_indices, positions, slot_mapping, block_table, state_cache, rms_w,
+                             eps: float, cos_sin_cache, k_cache, kv_slot_mapping, kv_block_size: int,
+                             stream=None) -> None:
+    """Test of the bounded waits (tests only): the C128 call with CTA 0's first stage never
+    filled, so the kernel gives up after its wait limit and reports C128_DEV_TIMEOUT (read it with
+    device_errors) instead of hanging. Needs more tokens than the GPU has SMs."""
+    L = lib()
+    descs = [describe(x) for x in (token_to_req_indices, positions, slot_mapping, block_table, state_cache, rms_w)]
+    cs, kc, kvs = describe(cos_sin_cache), describe(k_cache), describe(kv_slot_mapping)
+    rc = L.c128_debug_stall_first_window(*[ctypes.byref(a) for a in descs], ctypes.c_float(eps), ctypes.byref(cs),
+                                         ctypes.byref(kc), ctypes.byref(kvs), int(kv_block_size),
+                                         _stream_handle(stream))
+    _check(rc, "c128_debug_stall_first_window")
 
 
 def compress_norm_rope_store_noalloc(token_to_req_indices, positions, slot_mapping, block_table, state_cache,

@@ -243,9 +243,10 @@ int run(const c128_tensor_t* ttr, const c128_tensor_t* pos, const c128_tensor_t*
         const c128_tensor_t* bt, const c128_tensor_t* state, const c128_tensor_t* rms_w, float eps,
         const c128_tensor_t* cs, const c128_tensor_t* kc, const c128_tensor_t* kvslot,
         int64_t kv_block_size, const c128_tensor_t* comp_out, cudaStream_t stream,
-        const c128_config_t* config = nullptr) {
+        const c128_config_t* config = nullptr, bool stall_test = false) {
   c128::Params p{};
   C128_TRY(validate_call(ttr, pos, slot, bt, state, rms_w, eps, cs, kc, kvslot, kv_block_size, comp_out, &p, config));
+  p.stall_first_window = stall_test ? 1 : 0;
   const int64_t T = p.T;
   if (T == 0) return C128_OK;
 
@@ -258,6 +259,8 @@ int run(const c128_tensor_t* ttr, const c128_tensor_t* pos, const c128_tensor_t*
     C128_TRY(device_info(dev, &di));
     C128_TRY(workspace_for(dev, stream, T, &p.ws));
     cfg.sm_count = di->sm_count;
+    // the stall test needs the compress kernel: batches of more tokens than SMs
+    if (stall_test && T <= di->sm_count) return C128_ERR_ARG;
     const int64_t g = static_cast<int64_t>(di->sm_count) * di->ctas_per_sm;
     cfg.grid = static_cast<int>(T < g ? T : g);
     cfg.pdl = true;
@@ -301,6 +304,17 @@ int compress_norm_rope_store(const c128_tensor_t* token_to_req_indices, const c1
   return run(token_to_req_indices, positions, slot_mapping, block_table, state_cache, rms_w, eps,
              cos_sin_cache, k_cache, kv_slot_mapping, kv_block_size, nullptr,
              reinterpret_cast<cudaStream_t>(stream));
+}
+
+int c128_debug_stall_first_window(const c128_tensor_t* token_to_req_indices, const c128_tensor_t* positions,
+                                   const c128_tensor_t* slot_mapping, const c128_tensor_t* block_table,
+                                   const c128_tensor_t* state_cache, const c128_tensor_t* rms_w, float eps,
+                                   const c128_tensor_t* cos_sin_cache, const c128_tensor_t* k_cache,
+                                   const c128_tensor_t* kv_slot_mapping, int64_t kv_block_size,
+                                   c128_stream_t stream) {
+  return run(token_to_req_indices, positions, slot_mapping, block_table, state_cache, rms_w, eps,
+             cos_sin_cache, k_cache, kv_slot_mapping, kv_block_size, nullptr,
+             reinterpret_cast<cudaStream_t>(stream), nullptr, true);
 }
 
 int c128_compress_norm_rope_store_debug(const c128_tensor_t* token_to_req_indices,

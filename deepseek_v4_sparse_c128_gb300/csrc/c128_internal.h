@@ -73,6 +73,7 @@ struct Params {
   int32_t fmt;                // cache format (C128_FORMAT_*)
   int64_t sblk;               // state-cache block size (rows per block)
   int32_t strided;            // C128 kernel only: no planning pass, CTA c takes tokens c, c + grid, ...
+  int32_t stall_first_window; // test only: CTA 0 arms its first stage but never copies into it
 };
 
 // True for the configuration the specialised C128 kernels serve.

@@ -215,7 +215,10 @@ __device__ void copy_thread(const Params& p, Smem& S) {
       }
       mbar_arrive_expect_tx(&S.full[s], kStageBytes);
       const float* src = d.src[j];
-      if (block_contiguous) {
+      if (p.stall_first_window && blockIdx.x == 0 && it == 0) {
+        // test of the bounded waits: this stage never fills, so its consumers give up after the
+        // time limit and the kernel reports C128_DEV_TIMEOUT instead of hanging
+      } else if (block_contiguous) {
         bulk_copy_g2s(S.stage[s], src, kStageBytes, &S.full[s], policy);
       } else {
         for (int r = 0; r < kStateBlock; ++r)
