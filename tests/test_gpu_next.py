@@ -154,3 +154,31 @@ def test_padded_strides_generic(name):
     kc, comp, err = run_gpu_ex(p, dev=dev)
     assert err == 0
     check_against_oracle_ex(p, kc, comp)
+
+
+@pytest.mark.parametrize("name", ["c4_sparse", "idx_c4_fp8", "idx_c128_mxfp4"])
+def test_graph_capture_generic(name):
+    """The ring kernels (tensor map encoded on the host at launch) captured in a CUDA graph and
+    replayed give the eager call's bytes."""
+    import torch
+    from deepseek_v4_sparse_c128_gb300 import binding
+    p = inputs.make_next_problem(name)
+    kc_eager, _, err = run_gpu_ex(p, comp=False)
+    assert err == 0
+    d = to_device(p)
+    cfg = binding.config(p.head, p.ratio, p.overlap, p.state_width, p.fmt)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        binding.reserve_workspace(p.num_tokens)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        binding.compress_norm_rope_store_ex(cfg, d["token_to_req"], d["positions"], d["slot_mapping"],
+                                            d["block_table"], d["state"], d["rms_w"], p.eps, d["cos_sin"],
+                                            d["k_cache"], d["kv_slot_mapping"], p.kv_block_size)
+    for _ in range(2):
+        d["k_cache"].copy_(torch.from_numpy(p.k_cache).cuda())
+        g.replay()
+        torch.cuda.synchronize()
+        assert np.array_equal(d["k_cache"].cpu().numpy(), kc_eager)
+    assert binding.device_errors(s, clear=True) == 0

@@ -290,6 +290,31 @@ def test_streams_graphs_and_timer():
     assert ref is not None
 
 
+@pytest.mark.parametrize("tokens", [300, 2000])  # token striding; memset + planning pass + PDL
+def test_graph_capture_c128_paths(tokens):
+    import torch
+    from deepseek_v4_sparse_c128_gb300 import binding
+    p = inputs.make_problem("sweep", tokens=tokens)
+    kc_eager, _, err = run_gpu(p, comp=False)
+    assert err == 0
+    d = to_device(p)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        binding.reserve_workspace(p.num_tokens)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        binding.compress_norm_rope_store(d["token_to_req"], d["positions"], d["slot_mapping"], d["block_table"],
+                                         d["state"], d["rms_w"], p.eps, d["cos_sin"], d["k_cache"],
+                                         d["kv_slot_mapping"], p.kv_block_size)
+    for _ in range(2):
+        d["k_cache"].copy_(torch.from_numpy(p.k_cache).cuda())
+        g.replay()
+        torch.cuda.synchronize()
+        assert np.array_equal(d["k_cache"].cpu().numpy(), kc_eager)
+    assert binding.device_errors(s, clear=True) == 0
+
+
 def test_prepared_call_matches_function_call():
     import torch
     from deepseek_v4_sparse_c128_gb300 import binding
