@@ -10,10 +10,11 @@
 //                row (the older or the newer half of an overlapping window). Completion is
 //                counted in bytes on the stage's mbarrier.
 //   warps 2..9   consumers: row group g (two warps, thread i owns columns 2i, 2i+1) folds chunk g
-//                of every stage into an online softmax; after the window's last stage the four
-//                row groups' partial states are merged, in row-group order, by consumer warp 0,
-//                which runs the indexer epilogue (RMSNorm, RoPE, FP8 or MXFP4 cache store) while
-//                the other warps go on with the next window.
+//                of every stage into an online softmax; after the window's last stage they write
+//                the four row groups' partial states (double-buffered) and go on with the next
+//                window.
+//   warp 10      epilogue: merges the partial states in row-group order and runs the indexer
+//                epilogue (RMSNorm, RoPE, FP8 or MXFP4 cache store), so no consumer waits for it.
 //
 // Same arithmetic as the oracle's reading of _fused_kv_compress_norm_rope_insert_indexer_attn and
 // ..._indexer_mxfp4_attn on the API page of vllm.models.deepseek_v4.common.ops.fused_compress_quant_cache.
@@ -37,9 +38,12 @@ constexpr int kIxChunkFloats = kIxChunk * kIxRowFloats;                // 8 KiB
 constexpr int kIxStageFloats = kIxStageChunks * kIxChunkFloats;        // 32 KiB
 constexpr int kIxConsumerWarps = 8;
 constexpr int kIxConsumerThreads = 32 * kIxConsumerWarps;
-constexpr int kIxThreads = 32 * (2 + kIxConsumerWarps);
+constexpr int kIxThreads = 32 * (3 + kIxConsumerWarps);                // + the epilogue warp
 constexpr int kIxRowGroups = kIxStageChunks;                           // row group g takes chunk g of a stage
-constexpr int kIxDescSlots = 2;
+#ifndef C128_IX_DESC_SLOTS
+#define C128_IX_DESC_SLOTS 2
+#endif
+constexpr int kIxDescSlots = C128_IX_DESC_SLOTS;
 static_assert(kIxRowGroups * kIxHead / 2 == kIxConsumerThreads, "two columns per consumer thread");
 
 struct __align__(16) IxDesc {
@@ -66,6 +70,16 @@ struct IxSmem {
   alignas(16) float part_l[2][kIxRowGroups][kIxHead];
   alignas(16) float part_a[2][kIxRowGroups][kIxHead];
   alignas(16) float comp_s[kIxHead];  // exact-variance slow path of the epilogue warp (float4 stores)
+  struct PartMeta {
+    uint8_t* tok;
+    uint8_t* scale;
+    const float* cs_row;
+    float* comp_dst;
+    int32_t end;  // no more windows
+    int32_t pad[3];
+  } meta[2];
+  uint64_t pfull[2];   // a window's partials written (one arrival per consumer warp)
+  uint64_t pempty[2];  // the epilogue warp is done with them (one arrival)
   int abort_flag;
 };
 static_assert(sizeof(IxSmem) <= 227 * 1024, "shared memory");
@@ -97,11 +111,14 @@ __device__ void ix_scheduler(const Params& p, IxSmem& S, int lane) {
   const uint32_t A = static_cast<uint32_t>(min(static_cast<int64_t>(*reinterpret_cast<volatile unsigned*>(&p.ws->count)), p.T));
   const int n = (1 + p.overlap) * p.ratio;  // 16..256 rows, a multiple of 8
   uint32_t widx = 0;
+  bool first_claim = true;
   for (;;) {
     if (*abort_flag) return;
+    // the first window of CTA c is window c; later ones come from the shared counter
     uint32_t a = 0;
-    if (lane == 0) a = atomicAdd(&p.ws->next, 1u);
+    if (lane == 0) a = first_claim ? blockIdx.x : gridDim.x + atomicAdd(&p.ws->next, 1u);
     a = __shfl_sync(0xffffffffu, a, 0);
+    first_claim = false;
     const bool end = a >= A;
     long long t = 0, pos = 0, kvs = 0;
     int req = 0;
@@ -181,6 +198,8 @@ __device__ void ix_scheduler(const Params& p, IxSmem& S, int lane) {
 __device__ void ix_copier(const Params& p, IxSmem& S, const CUtensorMap* map) {
   const volatile int* abort_flag = &S.abort_flag;
   const uint64_t policy = l2_evict_first_policy();
+  // rows of kv[128] | score[128] one after the other: an 8-row chunk is one contiguous 8 KiB range
+  const bool linear = p.sw == kIxHead && p.s1 == kIxRowFloats;
   uint32_t it = 0, widx = 0;
   bool failed = false;
   for (;;) {
@@ -201,9 +220,15 @@ __device__ void ix_copier(const Params& p, IxSmem& S, const CUtensorMap* map) {
       }
       const int cnt = min(kIxStageChunks, nch - c0);
       mbar_arrive_expect_tx(&S.full[s], static_cast<uint32_t>(cnt * kIxChunkFloats * 4));
-      for (int j = 0; j < cnt; ++j)
-        ix_tma_load(S.stage[s] + j * kIxChunkFloats, map, d.half[c0 + j], d.row[c0 + j], d.blk[c0 + j], &S.full[s],
-                    policy);
+      for (int j = 0; j < cnt; ++j) {
+        if (linear)
+          bulk_copy_g2s(S.stage[s] + j * kIxChunkFloats,
+                        p.state + static_cast<int64_t>(d.blk[c0 + j]) * p.s0 + static_cast<int64_t>(d.row[c0 + j]) * p.s1,
+                        kIxChunkFloats * 4, &S.full[s], policy);
+        else
+          ix_tma_load(S.stage[s] + j * kIxChunkFloats, map, d.half[c0 + j], d.row[c0 + j], d.blk[c0 + j], &S.full[s],
+                      policy);
+      }
       ++it;
     }
     if (failed) break;
@@ -256,13 +281,10 @@ __device__ __forceinline__ void ix_fold_chunk(const float* st, int c0, Online& o
 
 template <int FMT>
 __device__ void ix_consumers(const Params& p, IxSmem& S, int ci) {
-  const int cw = ci >> 5, lane = ci & 31;
+  const int lane = ci & 31;
   const int rg = ci / (kIxHead / 2);     // row group: chunk rg of every stage
   const int c0 = 2 * (ci % (kIxHead / 2));
   const volatile int* abort_flag = &S.abort_flag;
-  // the epilogue warp (consumer warp 0): lane l owns columns 4l..4l+3
-  const float2 wa = *reinterpret_cast<const float2*>(p.rms_w + 4 * lane);
-  const float2 wb = *reinterpret_cast<const float2*>(p.rms_w + 4 * lane + 2);
   uint32_t it = 0, widx = 0;
   for (;;) {
     const int ds = widx % kIxDescSlots;
@@ -282,16 +304,26 @@ __device__ void ix_consumers(const Params& p, IxSmem& S, int ci) {
     } else {
       ix_set_timeout(p, &S.abort_flag);
     }
-    if (consumer_bar_or(!got || nch == 0 || *abort_flag)) return;
+    if (consumer_bar_or(!got || nch == 0 || *abort_flag)) {
+      // a clean end (every consumer saw the end marker, nothing aborted): tell the epilogue warp,
+      // through the next partials buffer, that no window follows
+      if (!consumer_bar_or(!got || *abort_flag)) {
+        const int pb = widx & 1;
+        const bool free_ok = __all_sync(
+            0xffffffffu, widx < 2 || mbar_wait_suspend(&S.pempty[pb], ((widx >> 1) - 1u) & 1u, abort_flag));
+        if (free_ok) {
+          if (ci == 0) S.meta[pb].end = 1;
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&S.pfull[pb]);
+        } else if (lane == 0) {
+          ix_set_timeout(p, &S.abort_flag);
+        }
+      }
+      return;
+    }
     __syncwarp();
     if (lane == 0) mbar_arrive(&S.dempty[ds]);  // the fields above are in registers
 
-    float2 cosv = make_float2(1.f, 1.f), sinv = make_float2(0.f, 0.f);
-    if (cw == 0 && lane >= 16) {  // pairs 2l, 2l + 1 >= 32 rotate
-      const int j0 = 2 * lane - 32;
-      cosv = make_float2(__ldg(cs_row + j0), __ldg(cs_row + j0 + 1));
-      sinv = make_float2(__ldg(cs_row + kRope / 2 + j0), __ldg(cs_row + kRope / 2 + j0 + 1));
-    }
     Online o;
     online_init(o);
     bool failed = false;
@@ -309,34 +341,63 @@ __device__ void ix_consumers(const Params& p, IxSmem& S, int ci) {
       ++it;
     }
     if (failed) ix_set_timeout(p, &S.abort_flag);
+    // hand the partial states to the epilogue warp (buffer widx & 1, free once it took window widx - 2)
     const int pb = widx & 1;
+    bool free_ok = widx < 2 || mbar_wait_suspend(&S.pempty[pb], ((widx >> 1) - 1u) & 1u, abort_flag);
+    if (consumer_bar_or(failed || !free_ok)) {
+      if (!free_ok) ix_set_timeout(p, &S.abort_flag);
+      return;
+    }
     *reinterpret_cast<float2*>(&S.part_m[pb][rg][c0]) = make_float2(o.m0, o.m1);
     *reinterpret_cast<float2*>(&S.part_l[pb][rg][c0]) = make_float2(o.l0, o.l1);
     *reinterpret_cast<float2*>(&S.part_a[pb][rg][c0]) = make_float2(o.a0, o.a1);
-    if (consumer_bar_or(failed)) return;  // partials written; every consumer agrees on the outcome
-    if (cw == 0) {
-      // merge the row groups in order, columns 4l..4l+3
-      float out[4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int col = 4 * lane + j;
-        float M = S.part_m[pb][0][col];
-#pragma unroll
-        for (int g = 1; g < kIxRowGroups; ++g) M = fmaxf(M, S.part_m[pb][g][col]);
-        const float B = M == -INFINITY ? 0.f : M;
-        float L = 0.f, Acc = 0.f;
-#pragma unroll
-        for (int g = 0; g < kIxRowGroups; ++g) {
-          const float sc = ex2_approx(S.part_m[pb][g][col] - B);
-          L = fmaf(S.part_l[pb][g][col], sc, L);
-          Acc = fmaf(S.part_a[pb][g][col], sc, Acc);
-        }
-        out[j] = __fdiv_rn(Acc, L);
-      }
-      indexer_warp_epilogue<FMT>(make_float4(out[0], out[1], out[2], out[3]), lane, wa, wb, p.eps, cosv, sinv, tok,
-                                 scale, comp_dst, S.comp_s);
-    }
+    if (ci == 0) S.meta[pb] = IxSmem::PartMeta{tok, scale, cs_row, comp_dst, 0, {0, 0, 0}};
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&S.pfull[pb]);
     ++widx;
+  }
+}
+
+// ------------------------------------------------------------------------------- epilogue warp
+template <int FMT>
+__device__ void ix_epilogue_warp(const Params& p, IxSmem& S, int lane) {
+  const volatile int* abort_flag = &S.abort_flag;
+  const float2 wa = *reinterpret_cast<const float2*>(p.rms_w + 4 * lane);  // lane l owns columns 4l..4l+3
+  const float2 wb = *reinterpret_cast<const float2*>(p.rms_w + 4 * lane + 2);
+  for (uint32_t widx = 0;; ++widx) {
+    const int pb = widx & 1;
+    const bool ok = mbar_wait_suspend(&S.pfull[pb], (widx >> 1) & 1u, abort_flag);
+    if (!__all_sync(0xffffffffu, ok)) return;  // the consumers stopped (a timeout already reported)
+    const IxSmem::PartMeta m = S.meta[pb];
+    if (m.end) return;
+    float2 cosv = make_float2(1.f, 1.f), sinv = make_float2(0.f, 0.f);
+    if (lane >= 16) {  // pairs 2l, 2l + 1 >= 32 rotate
+      const int j0 = 2 * lane - 32;
+      cosv = make_float2(__ldg(m.cs_row + j0), __ldg(m.cs_row + j0 + 1));
+      sinv = make_float2(__ldg(m.cs_row + kRope / 2 + j0), __ldg(m.cs_row + kRope / 2 + j0 + 1));
+    }
+    // merge the row groups in order, columns 4l..4l+3
+    float out[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int col = 4 * lane + j;
+      float M = S.part_m[pb][0][col];
+#pragma unroll
+      for (int g = 1; g < kIxRowGroups; ++g) M = fmaxf(M, S.part_m[pb][g][col]);
+      const float B = M == -INFINITY ? 0.f : M;
+      float L = 0.f, Acc = 0.f;
+#pragma unroll
+      for (int g = 0; g < kIxRowGroups; ++g) {
+        const float sc = ex2_approx(S.part_m[pb][g][col] - B);
+        L = fmaf(S.part_l[pb][g][col], sc, L);
+        Acc = fmaf(S.part_a[pb][g][col], sc, Acc);
+      }
+      out[j] = __fdiv_rn(Acc, L);
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&S.pempty[pb]);  // the partials are in registers
+    indexer_warp_epilogue<FMT>(make_float4(out[0], out[1], out[2], out[3]), lane, wa, wb, p.eps, cosv, sinv, m.tok,
+                               m.scale, m.comp_dst, S.comp_s);
   }
 }
 
@@ -355,6 +416,10 @@ __global__ void __launch_bounds__(kIxThreads, 1)
       mbar_init(&S.dfull[d], 1);
       mbar_init(&S.dempty[d], kIxConsumerWarps + 1);
     }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&S.pfull[b], kIxConsumerWarps);
+      mbar_init(&S.pempty[b], 1);
+    }
     S.abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -364,7 +429,10 @@ __global__ void __launch_bounds__(kIxThreads, 1)
   } else if (warp == 1) {
     if (lane == 0) ix_copier(p, S, &state_map);
   } else {
-    ix_consumers<FMT>(p, S, tid - 64);
+    if (warp < 2 + kIxConsumerWarps)
+      ix_consumers<FMT>(p, S, tid - 64);
+    else
+      ix_epilogue_warp<FMT>(p, S, lane);
   }
 }
 
