@@ -182,3 +182,29 @@ def test_graph_capture_generic(name):
         torch.cuda.synchronize()
         assert np.array_equal(d["k_cache"].cpu().numpy(), kc_eager)
     assert binding.device_errors(s, clear=True) == 0
+
+
+@pytest.mark.parametrize("name", NEXT)
+def test_next_bench_size_sampled(name):
+    """Each configuration at the size bench.py times (about a quarter million tokens, state drawn
+    on the device, larger than L2): the stored set equals the activity predicate, every stored
+    slot equals the oracle epilogue replayed on the GPU's comp32, and 256 sampled windows' comp32
+    match the oracle within 1e-6 + 1e-5|x|."""
+    import dataclasses
+    import bench
+    from gpu_util import comp_close, replay_expected_ex, NAN_BITS
+    p = inputs.make_next_problem(name, state_device="cuda", scale=bench.NEXT_SCALES[name])
+    kc, comp, err = run_gpu_ex(p, dev=to_device(p))
+    assert err == 0
+    ph = dataclasses.replace(p, state=p.state.cpu().numpy())
+    rows = written_rows(comp)
+    active = np.nonzero((p.slot_mapping >= 0) & (p.positions >= 0) & ((p.positions + 1) % p.ratio == 0) &
+                        (p.kv_slot_mapping >= 0))[0]
+    assert np.array_equal(rows, active)
+    assert np.array_equal(replay_expected_ex(ph, comp, rows), kc)
+    sample = np.sort(np.random.default_rng(5).choice(rows, size=min(256, rows.size), replace=False))
+    comp_ref = np.zeros((p.num_tokens, p.head), np.float32)
+    comp_ref.view(np.uint32)[:] = NAN_BITS
+    oracle.forward_ex(ph, k_cache=ph.k_cache.copy(), tokens=sample, comp_out=comp_ref, threads=16)
+    ok, max_abs, worst = comp_close(comp[sample], comp_ref[sample])
+    assert ok, (max_abs, worst)
