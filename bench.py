@@ -331,9 +331,14 @@ def run_ours(args, ws, rank, local):
         sub = oracle_sample_problem(p, sample, gather_blocks_to_host(p, p.state, sample))
         threads = os.cpu_count() or 1
         wps, passes, cpu_s = time_oracle(sub, threads)
+        # the same oracle on one thread, over the first 128 sampled windows (a few seconds)
+        sub1 = oracle_sample_problem(p, sample[:128], sub.state[:16 * 128])
+        wps1, passes1, _ = time_oracle(sub1, 1, min_cpu_s=3.0, max_wall_s=20.0)
         out["cpu_baseline"] = {"value": wps, "unit": UNIT, "cores": threads, "kind": "oracle",
                                "sample": f"{sample.size} random windows of sweep{T} x {passes} passes "
-                                         f"({cpu_s:.1f} s CPU), oracle over host threads"}
+                                         f"({cpu_s:.1f} s CPU), oracle over host threads",
+                               "single_thread": {"value": wps1, "unit": UNIT, "cores": 1,
+                                                 "sample": f"128 of those windows x {passes1} passes"}}
     if not args.no_next and ws == 1:
         out["other_configurations"] = bench_next(args, dev)
     if not args.no_sweep and ws == 1:
