@@ -142,18 +142,43 @@ def test_one_hot_epilogue_edges_generic(fmt, head, ratio, overlap):
     assert rep["e2e_bytes_differ"] == 0
 
 
-@pytest.mark.parametrize("name", ["idx_c4_mxfp4", "idx_c128_fp8", "c4_sparse"])
+@pytest.mark.parametrize("name", ["idx_c4_mxfp4", "idx_c128_fp8", "c4_sparse", "idx_c4_fp8"])
 def test_padded_strides_generic(name):
+    """Padded state rows, padded block-table rows, cos/sin rows of 66 floats (rows not 16-byte
+    aligned) and k_cache blocks wider than their records: the ring kernels address everything
+    through the strides."""
     import torch
+    from gpu_util import FORMAT_BYTES, replay_expected_ex
     p = inputs.make_next_problem(name)
     dev = to_device(p)
     NB, BS, RW = p.state.shape
     big = torch.zeros((NB, BS, RW + 36), dtype=torch.float32, device="cuda")
     big[:, :, :RW].copy_(dev["state"])
     dev["state"] = big[:, :, :RW]
+    R, MB = p.block_table.shape
+    bt = torch.zeros((R, MB + 5), dtype=torch.int32, device="cuda")
+    bt[:, :MB].copy_(dev["block_table"])
+    dev["block_table"] = bt[:, :MB]
+    MP = p.cos_sin.shape[0]
+    cs = torch.zeros((MP, 66), dtype=torch.float32, device="cuda")
+    cs[:, :64].copy_(dev["cos_sin"])
+    dev["cos_sin"] = cs[:, :64]
+    tb, sb = FORMAT_BYTES[p.fmt]
+    NKB, bs, W = p.k_cache.shape
+    Wp = tb + sb + 16
+    kbig = torch.randint(0, 256, (NKB, bs * Wp + 16), dtype=torch.uint8, device="cuda")
+    kview = kbig[:, :bs * Wp].view(NKB, bs, Wp)
+    kview.view(NKB, -1)[:, :bs * (tb + sb)].copy_(dev["k_cache"].view(NKB, -1))
+    before = kbig.cpu().numpy()
+    dev["k_cache"] = kview
     kc, comp, err = run_gpu_ex(p, dev=dev)
     assert err == 0
-    check_against_oracle_ex(p, kc, comp)
+    rows = written_rows(comp)
+    exp = before.copy()
+    exp[:, :bs * (tb + sb)] = replay_expected_ex(p, comp, rows).reshape(NKB, -1)
+    assert np.array_equal(kbig.cpu().numpy(), exp)
+    rep = check_against_oracle_ex(p, replay_expected_ex(p, comp, rows), comp)
+    assert rep["stored"] == rows.size > 0
 
 
 @pytest.mark.parametrize("name", ["c4_sparse", "idx_c4_fp8", "idx_c128_mxfp4"])
