@@ -52,18 +52,6 @@ __device__ __noinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const vol
     if (global_timer_ns() - t0 > kWaitTimeoutNs) return false;
   }
 }
-// Non-blocking test of a phase.
-__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred P;\n\t"
-      "mbarrier.test_wait.parity.shared::cta.b64 P, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, P;\n}"
-      : "=r"(ok)
-      : "r"(smem_addr(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
 // The same wait, but each retry lets the hardware suspend the thread until the phase completes
 // (at most kSuspendHintNs per try), so waiting warps take no issue slots from the warps that work.
 constexpr uint32_t kSuspendHintNs = 20000;
