@@ -692,3 +692,30 @@ def test_overlap_gather_and_masking():
             q = pos - 7 + pick
             want = p.block_table[r, q // 8].astype(np.float32) * 8 + q % 8 + np.where(pick >= 4, 0.5, 0.0)
             assert np.array_equal(comp[t], want.astype(np.float32)), t
+
+
+def test_indexer_absmax_floors():
+    """The absmax floors of the indexer formats, in closed form. MXFP4: a block whose values are
+    all zero has amax floored to 6*2^-126, RN32(6*2^-126 * RN32(1/6)) is exactly 2^-126 (the
+    product is 2^-126 (1 + 3e-8), below half an ulp), so e = -126, the UE8M0 byte is 1, and every
+    code is a zero (nibble 0 or 8, the sign of the zero). FP8 indexer: an all-zero vector has amax
+    floored to RN32(1e-4), and the scale is 2^e with e = ceil(log2(RN32(RN32(1e-4) RN32(1/448))))."""
+    rng = np.random.default_rng(64)
+    comp = rng.choice([-1.0, 1.0], 128).astype(np.float32)
+    w = rng.choice([0.5, 1.0, 2.0], 128).astype(np.float32)
+    w[32:64] = 0.0                                                    # block 1 is all zeros
+    cs = np.concatenate([np.ones(32, np.float32), np.zeros(32, np.float32)])
+    tok, sc = oracle.epilogue_indexer(2, comp, w, 0.0, cs)
+    assert sc[1] == 1
+    for byte in tok[16:32]:
+        assert (byte & 0xF) in (0, 8) and (byte >> 4) in (0, 8)
+    assert all(s != 1 for b, s in enumerate(sc) if b != 1)
+    # FP8 indexer, every value zero
+    tok8, sc8 = oracle.epilogue_indexer(1, comp, np.zeros(128, np.float32), 1e-6, cs)
+    floor = Fraction(float(np.float32(1e-4)))
+    raw = Fraction(float(rn32_of_fraction(floor * Fraction(float(np.float32(1 / 448))))))
+    e = math.ceil(math.log2(float(raw)))
+    if Fraction(2) ** (e - 1) >= raw:
+        e -= 1
+    assert sc8.view(np.float32)[0] == np.float32(2.0 ** e)
+    assert all(b in (0x00, 0x80) for b in tok8)
