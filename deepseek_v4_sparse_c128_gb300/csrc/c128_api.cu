@@ -195,7 +195,10 @@ int validate_call(const c128_tensor_t* ttr, const c128_tensor_t* pos, const c128
   if (kc->shape[2] < token_bytes(C.cache_format) + scale_bytes(C.cache_format)) return C128_ERR_SHAPE;
   if (kc->stride[2] != 1 || kc->stride[1] != kc->shape[2]) return C128_ERR_STRIDE;
   if (kc->shape[0] > 1 && kc->stride[0] < kc->shape[1] * kc->shape[2]) return C128_ERR_STRIDE;
-  if (kc->stride[0] % 8 != 0 || !aligned(kc->data, 16)) return C128_ERR_ALIGN;
+  // the widest k_cache store: 8 bytes (bf16 rope quads, sparse), 4 (e4m3 quads and the fp32 scale,
+  // indexer FP8), 2 (E2M1 byte pairs, MXFP4); block starts must keep that alignment
+  const int kc_align = C.cache_format == C128_FORMAT_SPARSE_FP8 ? 8 : C.cache_format == C128_FORMAT_INDEXER_FP8 ? 4 : 2;
+  if (kc->stride[0] % kc_align != 0 || !aligned(kc->data, 16)) return C128_ERR_ALIGN;
   C128_TRY(check_data(kc));
   // optional fp32 export [T, head]
   if (comp_out != nullptr) {

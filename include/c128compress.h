@@ -241,6 +241,9 @@ int c128_compress_norm_rope_store_noalloc(const c128_tensor_t* token_to_req_indi
  * (p / ratio) * ratio. k_cache blocks hold bs token records then bs scale records, as above.
  * comp_out, if not NULL, receives the fp32 compressed vectors ([T, head_dim], contiguous, 16-byte
  * aligned) of stored tokens.
+ * The k_cache block stride (stride[0], bytes) must be a multiple of 8 for the sparse format, 4 for
+ * the indexer FP8 format and 2 for MXFP4 (the widest store of each), which the natural layout
+ * bs x record bytes always is.
  * Everything else is as for compress_norm_rope_store; the C128 configuration (512, 64, 128, 0, 512,
  * sparse, state block 8) runs the same kernels as compress_norm_rope_store.
  * Returns C128_ERR_NULL_PTR for a NULL config and C128_ERR_UNSUPPORTED for a configuration outside

@@ -191,3 +191,80 @@ def test_inputs_module_holds_no_method_arithmetic():
     for word in ("softmax", "np.exp", "rsqrt", "sqrt", "e4m3", "bfloat16", "float8", "log2", "ceil("):
         assert word not in text, word
     assert np is not None
+
+
+def _ex_args(**over):
+    """A valid empty batch for compress_norm_rope_store_ex: the C4 indexer FP8 layout."""
+    I32, I64, F32, U8 = binding.C128_I32, binding.C128_I64, binding.C128_F32, binding.C128_U8
+    a = dict(cfg=binding.config(128, 4, 1, 256, 1), ttr=_t([0], I32), pos=_t([0], I64), slot=_t([0], I64),
+             bt=_t([4, 64], I32), state=_t([64, 8, 512], F32), rms=_t([128], F32), eps=1e-6, cs=_t([512, 64], F32),
+             kc=_t([4, 3, 132], U8), kvs=_t([0], I64), bs=3, comp=None)
+    a.update(over)
+    return a
+
+
+def _call_ex(L, a):
+    r = lambda x: ctypes.byref(x) if x is not None else None
+    return L.compress_norm_rope_store_ex(r(a["cfg"]), r(a["ttr"]), r(a["pos"]), r(a["slot"]), r(a["bt"]),
+                                         r(a["state"]), r(a["rms"]), ctypes.c_float(a["eps"]), r(a["cs"]), r(a["kc"]),
+                                         r(a["kvs"]), a["bs"], r(a["comp"]), None)
+
+
+@pytest.mark.parametrize("case,code", [
+    ("ok", 0), ("mxfp4_odd_block", 0), ("sparse_c4", 0), ("null_config", 1), ("kc_record_short", 3),
+    ("comp_width", 3), ("rope32", 6), ("sparse_head128", 6), ("indexer_head512", 6), ("format9", 6),
+    ("ratio3", 6), ("ratio512", 6), ("overlap2", 6), ("window_257_plus", 6), ("state_width_small", 6),
+    ("state_width_odd", 6), ("state_row_mismatch", 6), ("rms_width", 6), ("fp8_stride_not_4", 5),
+    ("sparse_stride_not_8", 5), ("mxfp4_stride_odd", 5),
+])
+def test_ex_validation_codes(L, case, code):
+    """Host checks of the configurable entry point (an empty batch: nothing is launched, so a
+    valid configuration returns 0 without a GPU)."""
+    I32, F32, U8 = binding.C128_I32, binding.C128_F32, binding.C128_U8
+    a = _ex_args()
+    if case == "mxfp4_odd_block":
+        a.update(cfg=binding.config(128, 4, 1, 256, 2), kc=_t([4, 3, 68], U8))
+    elif case == "sparse_c4":
+        a.update(cfg=binding.config(512, 4, 1, 1024, 0), state=_t([64, 8, 2048], F32), rms=_t([512], F32),
+                 kc=_t([4, 3, 584], U8))
+    elif case == "null_config":
+        a["cfg"] = None
+    elif case == "kc_record_short":
+        a["kc"] = _t([4, 3, 100], U8)
+    elif case == "comp_width":
+        a["comp"] = _t([0, 512], F32)
+    elif case == "rope32":
+        c = binding.config(128, 4, 1, 256, 1)
+        c.rope_head_dim = 32
+        a["cfg"] = c
+    elif case == "sparse_head128":
+        a["cfg"] = binding.config(128, 4, 1, 256, 0)
+    elif case == "indexer_head512":
+        a["cfg"] = binding.config(512, 4, 1, 1024, 1)
+    elif case == "format9":
+        a["cfg"] = binding.config(128, 4, 1, 256, 9)
+    elif case == "ratio3":
+        a["cfg"] = binding.config(128, 3, 1, 256, 1)
+    elif case == "ratio512":
+        a["cfg"] = binding.config(128, 512, 0, 256, 1)
+    elif case == "overlap2":
+        a["cfg"] = binding.config(128, 4, 2, 384, 1)
+    elif case == "window_257_plus":
+        a["cfg"] = binding.config(128, 256, 1, 256, 1)
+    elif case == "state_width_small":
+        a["cfg"] = binding.config(128, 4, 1, 128, 1)
+    elif case == "state_width_odd":
+        a.update(cfg=binding.config(128, 4, 1, 258, 1), state=_t([64, 8, 516], F32))
+    elif case == "state_row_mismatch":
+        a["state"] = _t([64, 8, 1024], F32)
+    elif case == "rms_width":
+        a["rms"] = _t([512], F32)
+    elif case == "fp8_stride_not_4":
+        a["kc"] = _t([4, 1, 133], U8)
+        a["bs"] = 1
+    elif case == "sparse_stride_not_8":
+        a.update(cfg=binding.config(512, 4, 1, 1024, 0), state=_t([64, 8, 2048], F32), rms=_t([512], F32),
+                 kc=_t([4, 1, 588], U8), bs=1)
+    elif case == "mxfp4_stride_odd":
+        a.update(cfg=binding.config(128, 4, 1, 256, 2), kc=_t([4, 1, 69], U8), bs=1)
+    assert _call_ex(L, a) == code
