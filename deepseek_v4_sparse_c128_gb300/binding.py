@@ -29,6 +29,7 @@ EXPORTS = (
     "c128_compress_norm_rope_store_noalloc",
     "compress_norm_rope_store_ex",
     "c128_debug_stall_first_window",
+    "c128_debug_stall_first_window_ex",
     "c128_status_string",
     "c128_reserve_workspace",
     "c128_device_errors",
@@ -93,6 +94,8 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     L.c128_compress_norm_rope_store_debug.argtypes = [T, T, T, T, T, T, ctypes.c_float, T, T, T, i64, T, vp]
     L.c128_compress_norm_rope_store_noalloc.argtypes = [T, T, T, T, T, T, ctypes.c_float, T, T, T, i64, vp]
     L.c128_debug_stall_first_window.argtypes = [T, T, T, T, T, T, ctypes.c_float, T, T, T, i64, vp]
+    L.c128_debug_stall_first_window_ex.argtypes = [ctypes.POINTER(Config), T, T, T, T, T, T, ctypes.c_float, T, T,
+                                                   T, i64, vp]
     L.compress_norm_rope_store_ex.argtypes = [ctypes.POINTER(Config), T, T, T, T, T, T, ctypes.c_float, T, T, T, i64,
                                               T, vp]
     L.c128_status_string.argtypes = [ctypes.c_int]
@@ -205,6 +208,20 @@ def debug_stall_first_window(token_to_req_indices, positions, slot_mapping, bloc
                                          ctypes.byref(kc), ctypes.byref(kvs), int(kv_block_size),
                                          _stream_handle(stream))
     _check(rc, "c128_debug_stall_first_window")
+
+
+def debug_stall_first_window_ex(cfg, token_to_req_indices, positions, slot_mapping, block_table, state_cache,
+                                rms_w, eps: float, cos_sin_cache, k_cache, kv_slot_mapping, kv_block_size: int,
+                                stream=None) -> None:
+    """The same test of the bounded waits for compress_norm_rope_store_ex (tests only): CTA 0 of
+    the small-window or indexer kernel leaves its first stage unfilled."""
+    L = lib()
+    descs = [describe(x) for x in (token_to_req_indices, positions, slot_mapping, block_table, state_cache, rms_w)]
+    cs, kc, kvs = describe(cos_sin_cache), describe(k_cache), describe(kv_slot_mapping)
+    rc = L.c128_debug_stall_first_window_ex(ctypes.byref(cfg), *[ctypes.byref(a) for a in descs], ctypes.c_float(eps),
+                                            ctypes.byref(cs), ctypes.byref(kc), ctypes.byref(kvs), int(kv_block_size),
+                                            _stream_handle(stream))
+    _check(rc, "c128_debug_stall_first_window_ex")
 
 
 def compress_norm_rope_store_noalloc(token_to_req_indices, positions, slot_mapping, block_table, state_cache,

@@ -262,8 +262,8 @@ int run(const c128_tensor_t* ttr, const c128_tensor_t* pos, const c128_tensor_t*
     C128_TRY(device_info(dev, &di));
     C128_TRY(workspace_for(dev, stream, T, &p.ws));
     cfg.sm_count = di->sm_count;
-    // the stall test needs the compress kernel: batches of more tokens than SMs
-    if (stall_test && T <= di->sm_count) return C128_ERR_ARG;
+    // the C128 stall test needs the compress kernel: batches of more tokens than SMs
+    if (stall_test && config == nullptr && T <= di->sm_count) return C128_ERR_ARG;
     const int64_t g = static_cast<int64_t>(di->sm_count) * di->ctas_per_sm;
     cfg.grid = static_cast<int>(T < g ? T : g);
     cfg.pdl = true;
@@ -318,6 +318,18 @@ int c128_debug_stall_first_window(const c128_tensor_t* token_to_req_indices, con
   return run(token_to_req_indices, positions, slot_mapping, block_table, state_cache, rms_w, eps,
              cos_sin_cache, k_cache, kv_slot_mapping, kv_block_size, nullptr,
              reinterpret_cast<cudaStream_t>(stream), nullptr, true);
+}
+
+int c128_debug_stall_first_window_ex(const c128_config_t* config, const c128_tensor_t* token_to_req_indices,
+                                      const c128_tensor_t* positions, const c128_tensor_t* slot_mapping,
+                                      const c128_tensor_t* block_table, const c128_tensor_t* state_cache,
+                                      const c128_tensor_t* rms_w, float eps, const c128_tensor_t* cos_sin_cache,
+                                      const c128_tensor_t* k_cache, const c128_tensor_t* kv_slot_mapping,
+                                      int64_t kv_block_size, c128_stream_t stream) {
+  if (config == nullptr) return C128_ERR_NULL_PTR;
+  return run(token_to_req_indices, positions, slot_mapping, block_table, state_cache, rms_w, eps,
+             cos_sin_cache, k_cache, kv_slot_mapping, kv_block_size, nullptr,
+             reinterpret_cast<cudaStream_t>(stream), config, true);
 }
 
 int c128_compress_norm_rope_store_debug(const c128_tensor_t* token_to_req_indices,

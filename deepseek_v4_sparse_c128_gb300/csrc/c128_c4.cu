@@ -90,7 +90,8 @@ struct __align__(16) SmallDesc {
   int32_t g_blk[2];                 // tiled path: state block, first row in it and half of each group
   int32_t g_row[2];
   int32_t g_half[2];
-  int32_t pad[3];
+  int32_t stall;                    // test only: leave this window's stage unfilled
+  int32_t pad[2];
 };
 
 template <int HEAD>
@@ -247,6 +248,7 @@ __device__ void small_scheduler(const Params& p, SmallSmem<HEAD>& S, int lane, b
       d.g_blk[1] = blk1;
       d.g_row[1] = row1;
       d.g_half[1] = half1;
+      d.stall = p.stall_first_window && a == 0;  // the first window of the list
       if (!tiled) {
         bool bad = false;
 #pragma unroll
@@ -327,7 +329,10 @@ __device__ void small_copier(const Params& p, SmallSmem<HEAD>& S, int lane, cons
             pass_slot = sl;
             pass_k = kk;
             float* st = S.stage[sl];
-            if (tiled) {
+            if (e.stall) {
+              // test of the bounded waits: this stage never fills, so its group gives up after the
+              // time limit and the kernel reports C128_DEV_TIMEOUT instead of hanging
+            } else if (tiled) {
               // box {cw, head/cw, 2, ratio, 1}: per row the kv half-row, then the score half-row
               const int ng = e.ngroups;
               for (int g = 0; g < ng; ++g)

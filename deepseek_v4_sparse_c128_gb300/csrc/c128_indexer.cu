@@ -220,7 +220,9 @@ __device__ void ix_copier(const Params& p, IxSmem& S, const CUtensorMap* map) {
       }
       const int cnt = min(kIxStageChunks, nch - c0);
       mbar_arrive_expect_tx(&S.full[s], static_cast<uint32_t>(cnt * kIxChunkFloats * 4));
-      for (int j = 0; j < cnt; ++j) {
+      // test of the bounded waits: CTA 0's first stage never fills
+      const int issue = p.stall_first_window && blockIdx.x == 0 && it == 0 ? 0 : cnt;
+      for (int j = 0; j < issue; ++j) {
         if (linear)
           bulk_copy_g2s(S.stage[s] + j * kIxChunkFloats,
                         p.state + static_cast<int64_t>(d.blk[c0 + j]) * p.s0 + static_cast<int64_t>(d.row[c0 + j]) * p.s1,

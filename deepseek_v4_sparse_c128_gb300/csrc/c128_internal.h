@@ -73,7 +73,9 @@ struct Params {
   int32_t fmt;                // cache format (C128_FORMAT_*)
   int64_t sblk;               // state-cache block size (rows per block)
   int32_t strided;            // C128 kernel only: no planning pass, CTA c takes tokens c, c + grid, ...
-  int32_t stall_first_window; // test only: CTA 0 arms its first stage but never copies into it
+  int32_t stall_first_window; // test only: one stage is armed but never filled (CTA 0's first in
+                              // the compress and indexer kernels, the first listed window's in the
+                              // small-window kernel)
 };
 
 // True for the configuration the specialised C128 kernels serve.

@@ -283,6 +283,29 @@ int compress_norm_rope_store_ex(const c128_config_t* config,
                                 const c128_tensor_t* comp_out,
                                 c128_stream_t stream);
 
+/*
+ * The same test for the other configurations (tests only): compress_norm_rope_store_ex with the
+ * small-window kernel (windows of at most 8 rows) leaving the stage of the first listed window
+ * unfilled, or the indexer kernel (head-128 windows of more than 8 rows) leaving CTA 0's first
+ * stage unfilled, with the same outcome:
+ * C128_DEV_TIMEOUT in the device error bits, the other CTAs' windows stored, the context usable.
+ * Configurations served by the gather kernel (no copy warp) run normally. Returns the codes of
+ * compress_norm_rope_store_ex.
+ */
+int c128_debug_stall_first_window_ex(const c128_config_t* config,
+                                     const c128_tensor_t* token_to_req_indices,
+                                     const c128_tensor_t* positions,
+                                     const c128_tensor_t* slot_mapping,
+                                     const c128_tensor_t* block_table,
+                                     const c128_tensor_t* state_cache,
+                                     const c128_tensor_t* rms_w,
+                                     float eps,
+                                     const c128_tensor_t* cos_sin_cache,
+                                     const c128_tensor_t* k_cache,
+                                     const c128_tensor_t* kv_slot_mapping,
+                                     int64_t kv_block_size,
+                                     c128_stream_t stream);
+
 /* Human-readable name of a return code (static string, never NULL). */
 const char* c128_status_string(int status);
 
