@@ -159,6 +159,10 @@ __device__ void small_scheduler(const Params& p, SmallSmem<HEAD>& S, int lane, b
   const volatile int* abort_flag = &S.abort_flag;
   const uint32_t A = static_cast<uint32_t>(min(static_cast<int64_t>(*reinterpret_cast<volatile unsigned*>(&p.ws->count)), p.T));
   const int n = (1 + p.overlap) * p.ratio;  // <= 8
+  // claim size: 32 windows when there is plenty of work, else about one claim per CTA, so that a
+  // small batch spreads over the SMs instead of a few CTAs taking 32 windows each
+  const uint32_t per_cta = (A + gridDim.x - 1) / gridDim.x;
+  const uint32_t batch = per_cta >= static_cast<uint32_t>(kBatch) ? static_cast<uint32_t>(kBatch) : max(per_cta, 1u);
   bool failed = false;
   for (uint32_t b = 0;; ++b) {
     const int qs = b & 1;
@@ -170,7 +174,7 @@ __device__ void small_scheduler(const Params& p, SmallSmem<HEAD>& S, int lane, b
       }
     }
     uint32_t base = 0;
-    if (lane == 0) base = atomicAdd(&p.ws->next, static_cast<unsigned>(kBatch));
+    if (lane == 0) base = atomicAdd(&p.ws->next, batch);
     base = __shfl_sync(0xffffffffu, base, 0);
     if (base >= A) {
       if (lane == 0) S.qcount[qs] = -1;
@@ -179,7 +183,7 @@ __device__ void small_scheduler(const Params& p, SmallSmem<HEAD>& S, int lane, b
     }
     // every lane resolves one window
     const uint32_t a = base + lane;
-    bool live = a < A;
+    bool live = a < A && static_cast<uint32_t>(lane) < batch;
     int64_t t = 0, pos = 0, kvs = 0, cp = 0, start = 0, first = 0;
     int req = 0, nvalid = 0, ngroups = 0;
     int blk0 = 0, row0 = 0, half0 = 0, blk1 = 0, row1 = 0, half1 = 0;
