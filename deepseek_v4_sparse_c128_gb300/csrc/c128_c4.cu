@@ -154,15 +154,21 @@ __device__ __forceinline__ void set_timeout(const Params& p, int* abort_flag) {
 // ------------------------------------------------------------------------------ scheduler warp
 template <int HEAD, int FMT>
 __device__ void small_scheduler(const Params& p, SmallSmem<HEAD>& S, int lane, bool tiled) {
-  grid_dependency_wait();  // the list and the counters come from plan_kernel
+  // list mode: windows from plan_kernel's list; token striding (few tokens, no planning pass):
+  // this CTA tests tokens c, c + grid, ..., 32 candidates per step
+  const bool strided = p.strided != 0;
+  if (!strided) grid_dependency_wait();  // the list and the counters come from plan_kernel
   const int32_t* list = reinterpret_cast<const int32_t*>(p.ws + 1);
   const volatile int* abort_flag = &S.abort_flag;
-  const uint32_t A = static_cast<uint32_t>(min(static_cast<int64_t>(*reinterpret_cast<volatile unsigned*>(&p.ws->count)), p.T));
+  const uint32_t A =
+      strided ? 0u : static_cast<uint32_t>(min(static_cast<int64_t>(*reinterpret_cast<volatile unsigned*>(&p.ws->count)), p.T));
   const int n = (1 + p.overlap) * p.ratio;  // <= 8
   // claim size: 32 windows when there is plenty of work, else about one claim per CTA, so that a
   // small batch spreads over the SMs instead of a few CTAs taking 32 windows each
   const uint32_t per_cta = (A + gridDim.x - 1) / gridDim.x;
   const uint32_t batch = per_cta >= static_cast<uint32_t>(kBatch) ? static_cast<uint32_t>(kBatch) : max(per_cta, 1u);
+  int64_t next_t = blockIdx.x;
+  bool stall_pending = strided && p.stall_first_window && blockIdx.x == 0;
   bool failed = false;
   for (uint32_t b = 0;; ++b) {
     const int qs = b & 1;
@@ -174,22 +180,33 @@ __device__ void small_scheduler(const Params& p, SmallSmem<HEAD>& S, int lane, b
       }
     }
     uint32_t base = 0;
-    if (lane == 0) base = atomicAdd(&p.ws->next, batch);
+    if (!strided && lane == 0) base = atomicAdd(&p.ws->next, batch);
     base = __shfl_sync(0xffffffffu, base, 0);
-    if (base >= A) {
+    if (strided ? next_t >= p.T : base >= A) {
       if (lane == 0) S.qcount[qs] = -1;
       mbar_arrive(&S.qfull[qs]);
       break;
     }
     // every lane resolves one window
     const uint32_t a = base + lane;
-    bool live = a < A && static_cast<uint32_t>(lane) < batch;
+    bool live;
     int64_t t = 0, pos = 0, kvs = 0, cp = 0, start = 0, first = 0;
+    if (strided) {
+      t = next_t + static_cast<int64_t>(lane) * gridDim.x;
+      next_t += 32ll * gridDim.x;
+      live = false;
+      if (t < p.T) {
+        const int64_t sl = __ldg(p.slot + t), ps = __ldg(p.pos + t), kv = __ldg(p.kvslot + t);
+        live = (sl >= 0) & (ps >= 0) & (((ps + 1) & (p.ratio - 1)) == 0) & (kv >= 0);
+      }
+    } else {
+      live = a < A && static_cast<uint32_t>(lane) < batch;
+      if (live) t = list[a];
+    }
     int req = 0, nvalid = 0, ngroups = 0;
     int blk0 = 0, row0 = 0, half0 = 0, blk1 = 0, row1 = 0, half1 = 0;
     uint32_t err = 0;
     if (live) {
-      t = list[a];
       req = __ldg(p.ttr + t);
       pos = __ldg(p.pos + t);
       kvs = __ldg(p.kvslot + t);
@@ -252,7 +269,8 @@ __device__ void small_scheduler(const Params& p, SmallSmem<HEAD>& S, int lane, b
       d.g_blk[1] = blk1;
       d.g_row[1] = row1;
       d.g_half[1] = half1;
-      d.stall = p.stall_first_window && a == 0;  // the first window of the list
+      // test only: the first window of the list, or CTA 0's first window when striding
+      d.stall = p.stall_first_window && (strided ? stall_pending && rank == 0 : a == 0);
       if (!tiled) {
         bool bad = false;
 #pragma unroll
@@ -278,6 +296,7 @@ __device__ void small_scheduler(const Params& p, SmallSmem<HEAD>& S, int lane, b
         }
       }
     }
+    if (live_mask) stall_pending = false;
     if (lane == 0) S.qcount[qs] = __popc(live_mask);
     mbar_arrive(&S.qfull[qs]);
   }

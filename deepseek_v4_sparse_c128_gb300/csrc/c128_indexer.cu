@@ -105,27 +105,54 @@ __device__ __forceinline__ void ix_tma_load(void* dst, const CUtensorMap* map, i
 template <int FMT>
 __device__ void ix_scheduler(const Params& p, IxSmem& S, int lane) {
   constexpr int kTok = FMT == C128_FORMAT_INDEXER_FP8 ? 128 : 64;
-  grid_dependency_wait();  // the list and the counters come from plan_kernel
+  // list mode: windows from plan_kernel's list; token striding (few tokens, no planning pass):
+  // this CTA tests tokens c, c + grid, ..., 32 candidates per step
+  const bool strided = p.strided != 0;
+  if (!strided) grid_dependency_wait();  // the list and the counters come from plan_kernel
   const int32_t* list = reinterpret_cast<const int32_t*>(p.ws + 1);
   const volatile int* abort_flag = &S.abort_flag;
-  const uint32_t A = static_cast<uint32_t>(min(static_cast<int64_t>(*reinterpret_cast<volatile unsigned*>(&p.ws->count)), p.T));
+  const uint32_t A =
+      strided ? 0u : static_cast<uint32_t>(min(static_cast<int64_t>(*reinterpret_cast<volatile unsigned*>(&p.ws->count)), p.T));
+  int64_t next_t = blockIdx.x;
   const int n = (1 + p.overlap) * p.ratio;  // 16..256 rows, a multiple of 8
   uint32_t widx = 0;
   bool first_claim = true;
   for (;;) {
     if (*abort_flag) return;
-    // the first window of CTA c is window c; later ones come from the shared counter
-    uint32_t a = 0;
-    if (lane == 0) a = first_claim ? blockIdx.x : gridDim.x + atomicAdd(&p.ws->next, 1u);
-    a = __shfl_sync(0xffffffffu, a, 0);
-    first_claim = false;
-    const bool end = a >= A;
+    bool end;
     long long t = 0, pos = 0, kvs = 0;
+    if (strided) {
+      long long found = -1;
+      while (found < 0 && next_t < p.T) {
+        const int64_t c = next_t + static_cast<int64_t>(lane) * gridDim.x;
+        bool act = false;
+        if (c < p.T) {
+          const int64_t sl = __ldg(p.slot + c), ps = __ldg(p.pos + c), kv = __ldg(p.kvslot + c);
+          act = (sl >= 0) & (ps >= 0) & (((ps + 1) & (p.ratio - 1)) == 0) & (kv >= 0);
+        }
+        const uint32_t m = __ballot_sync(0xffffffffu, act);
+        if (m) {
+          found = next_t + static_cast<int64_t>(__ffs(m) - 1) * gridDim.x;
+          next_t = found + gridDim.x;
+        } else {
+          next_t += 32ll * gridDim.x;
+        }
+      }
+      end = found < 0;
+      t = found;
+    } else {
+      // the first window of CTA c is window c; later ones come from the shared counter
+      uint32_t a = 0;
+      if (lane == 0) a = first_claim ? blockIdx.x : gridDim.x + atomicAdd(&p.ws->next, 1u);
+      a = __shfl_sync(0xffffffffu, a, 0);
+      first_claim = false;
+      end = a >= A;
+      if (!end && lane == 0) t = list[a];
+    }
     int req = 0;
     uint32_t err = 0;
     if (!end) {
       if (lane == 0) {
-        t = list[a];
         req = __ldg(p.ttr + t);
         pos = __ldg(p.pos + t);
         kvs = __ldg(p.kvslot + t);

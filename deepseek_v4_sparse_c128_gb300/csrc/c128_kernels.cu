@@ -581,7 +581,21 @@ cudaError_t prepare_device(int /*device*/) {
 
 cudaError_t launch(const Params& p, const LaunchCfg& cfg, cudaStream_t stream) {
   if (!is_c128(p)) {
-    cudaError_t e = cudaMemsetAsync(p.ws, 0, 2 * sizeof(unsigned int), stream);  // count, next
+    cudaError_t e;
+    if (p.T <= static_cast<int64_t>(kStridedTokensPerSm) * cfg.sm_count) {
+      // few tokens per SM: the ring kernels stride over the tokens themselves (no planning pass,
+      // no counters); configurations the gather kernel serves still take the planned path
+      Params q = p;
+      q.strided = 1;
+      if (cfg.ev_begin != nullptr && (e = cudaEventRecord(cfg.ev_begin, stream)) != cudaSuccess) return e;
+      e = small_window_path(q) ? launch_small(q, cfg, stream) : launch_indexer_windows(q, cfg, stream);
+      if (e != cudaErrorNotSupported) {
+        if (e != cudaSuccess) return e;
+        if (cfg.ev_end != nullptr) e = cudaEventRecord(cfg.ev_end, stream);
+        return e;
+      }
+    }
+    e = cudaMemsetAsync(p.ws, 0, 2 * sizeof(unsigned int), stream);  // count, next
     if (e != cudaSuccess) return e;
     const int plan_grid = static_cast<int>((p.T + kPlanTokensPerCta - 1) / kPlanTokensPerCta);
     plan_kernel<<<plan_grid, kPlanThreads, 0, stream>>>(p);
