@@ -104,19 +104,29 @@ __device__ void scheduler_warp(const Params& p, Smem& S, int lane) {
     int req = 0;
     uint32_t err = 0;
     if (strided) {
-      // the next active token among next_t, next_t + grid, ...: 32 candidates per step
+      // the next active token among next_t, next_t + grid, ...: 32 candidates per step; the
+      // candidates' request, position and kv slot come with the test, from the lane that found it
       long long found = -1;
       while (found < 0 && next_t < p.T) {
         const int64_t c = next_t + static_cast<int64_t>(lane) * gridDim.x;
         bool act = false;
+        long long ps = 0, kv = 0;
+        int rq = 0;
         if (c < p.T) {
-          const int64_t s = __ldg(p.slot + c), ps = __ldg(p.pos + c), kv = __ldg(p.kvslot + c);
+          const int64_t s = __ldg(p.slot + c);
+          ps = __ldg(p.pos + c);
+          kv = __ldg(p.kvslot + c);
+          rq = __ldg(p.ttr + c);
           act = (s >= 0) & (ps >= 0) & (((ps + 1) & (kRatio - 1)) == 0) & (kv >= 0);
         }
         const uint32_t m = __ballot_sync(0xffffffffu, act);
         if (m) {
-          found = next_t + static_cast<int64_t>(__ffs(m) - 1) * gridDim.x;
+          const int src = __ffs(m) - 1;
+          found = next_t + static_cast<int64_t>(src) * gridDim.x;
           next_t = found + gridDim.x;
+          pos = __shfl_sync(0xffffffffu, ps, src);
+          kvs = __shfl_sync(0xffffffffu, kv, src);
+          req = __shfl_sync(0xffffffffu, rq, src);
         } else {
           next_t += 32ll * gridDim.x;
         }
@@ -132,9 +142,11 @@ __device__ void scheduler_warp(const Params& p, Smem& S, int lane) {
     }
     if (!end) {
       if (lane == 0) {
-        req = __ldg(p.ttr + t);
-        pos = __ldg(p.pos + t);
-        kvs = __ldg(p.kvslot + t);
+        if (!strided) {
+          req = __ldg(p.ttr + t);
+          pos = __ldg(p.pos + t);
+          kvs = __ldg(p.kvslot + t);
+        }
         if (req < 0 || req >= p.bt_rows) err |= C128_DEV_BAD_REQ;
         if (pos / kStateBlock >= p.bt_cols) err |= C128_DEV_BAD_BT_COL;
         if (pos - (kRatio - 1) >= p.cs_rows) err |= C128_DEV_BAD_COS_ROW;  // (p/128)*128 == p-127
@@ -383,6 +395,10 @@ __global__ void __launch_bounds__(kThreads, 1) direct_kernel(Params p) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t rank = S > 1 ? cluster_ctarank() : 0u;
   const int64_t t = static_cast<int64_t>(blockIdx.x) / S;
+  // the token (every thread; broadcast loads), issued before the barrier set-up so that their
+  // latency overlaps it
+  const int64_t slot = __ldg(p.slot + t), pos = __ldg(p.pos + t), kvs = __ldg(p.kvslot + t);
+  const int req = __ldg(p.ttr + t);
   if (tid == 0) {
     for (int s = 0; s < Cfg::kRing; ++s) {
       mbar_init(&D.full[s], 1);
@@ -395,10 +411,8 @@ __global__ void __launch_bounds__(kThreads, 1) direct_kernel(Params p) {
   __syncthreads();
   const volatile int* abort_flag = &D.abort_flag;
 
-  // the token and its window (every thread; broadcast loads)
-  const int64_t slot = __ldg(p.slot + t), pos = __ldg(p.pos + t), kvs = __ldg(p.kvslot + t);
+  // the token's window
   if (!((slot >= 0) & (pos >= 0) & ((pos & (kRatio - 1)) == kRatio - 1) & (kvs >= 0))) return;
-  const int req = __ldg(p.ttr + t);
   uint32_t err = 0;
   if (req < 0 || req >= p.bt_rows) err |= C128_DEV_BAD_REQ;
   if (pos / kStateBlock >= p.bt_cols) err |= C128_DEV_BAD_BT_COL;
