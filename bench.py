@@ -324,6 +324,11 @@ def run_ours(args, ws, rank, local):
                        "traffic": traffic_per_launch(T), "kernel_us": kernel_ms * 1e3,
                        "algorithmic_bytes_per_launch": T * ALGO_BYTES_PER_WINDOW}
     out["clocks"] = clocks.summary()
+    if not args.no_read_probe:
+        probe = read_probe_rate(d["state"], stream)
+        out["hbm_read_probe"] = probe
+        out["roofline"]["read_probe_gbs"] = probe["gbs"]
+        out["roofline"]["frac_of_read_probe"] = achieved / probe["gbs"]
 
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         rng = np.random.default_rng(11)
@@ -347,6 +352,38 @@ def run_ours(args, ws, rank, local):
         out["sweep_us_per_call"] = sweep(args, dev)
     if rank == 0:
         print(json.dumps(out), flush=True)
+
+
+READ_PROBE_SHAPES = ((1024, 1, 8), (512, 2, 8), (512, 2, 4), (256, 4, 8), (1024, 2, 4), (512, 4, 4))
+
+
+def read_probe_rate(buf, stream, launches: int = 10) -> dict:
+    """DRAM read rate of a plain streaming read (c128_read_probe) over the whole buffer ``buf``
+    (larger than L2), best over a few launch shapes; CUDA events on ``stream``."""
+    import torch
+    from deepseek_v4_sparse_c128_gb300 import binding
+    word = torch.zeros(1, dtype=torch.int32, device=buf.device)
+    nbytes = buf.numel() * buf.element_size()
+    rates = {}
+    for threads, ctas, loads in READ_PROBE_SHAPES:
+        for _ in range(2):
+            binding.read_probe(buf, word, threads, ctas, loads, stream=stream)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(launches):
+            binding.read_probe(buf, word, threads, ctas, loads, stream=stream)
+        b.record(stream)
+        b.synchronize()
+        rates[f"{threads}x{ctas}x{loads}"] = nbytes * launches / (a.elapsed_time(b) * 1e-3) / 1e9
+    best = max(rates, key=rates.get)
+    t, c, l = (int(x) for x in best.split("x"))
+    return {"gbs": rates[best], "unit": "GB/s", "bytes": nbytes,
+            "shape": {"threads_per_cta": t, "ctas_per_sm": c, "loads_in_flight": l},
+            "all_shapes_gbs": {k: round(v, 1) for k, v in rates.items()},
+            "how": f"c128_read_probe: one pass of 16-byte streaming loads over the {nbytes / 1e9:.2f} GB state "
+                   f"buffer (> L2) per launch, {launches} launches per shape (threads per CTA x CTAs per SM x "
+                   f"loads in flight per thread) after 2 warm-ups, CUDA events, best shape; right after the "
+                   f"timed region"}
 
 
 def launches_per_call(T: int, sm_count: int) -> int:
@@ -631,6 +668,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-next", action="store_true")
+    ap.add_argument("--no-read-probe", action="store_true")
     ap.add_argument("--case", choices=["sweep"] + list(NEXT_SCALES),
                     help="run one workload alone (no JSON bench line); used for profiling")
     args = ap.parse_args()

@@ -36,6 +36,7 @@ EXPORTS = (
     "c128_kernel_timer_begin",
     "c128_kernel_timer_end",
     "c128_get_info",
+    "c128_read_probe",
     "c128_release_all",
 )
 
@@ -105,6 +106,8 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     L.c128_kernel_timer_begin.argtypes = [vp]
     L.c128_kernel_timer_end.argtypes = [vp, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int64)]
     L.c128_get_info.argtypes = [ctypes.POINTER(Info)]
+    i32 = ctypes.c_int32
+    L.c128_read_probe.argtypes = [vp, i64, i32, i32, i32, vp, vp]
     L.c128_release_all.argtypes = []
     for name in EXPORTS:
         if name != "c128_status_string":
@@ -322,6 +325,18 @@ def info() -> dict:
     i = Info()
     _check(lib().c128_get_info(ctypes.byref(i)), "c128_get_info")
     return {f: getattr(i, f) for f, _ in Info._fields_}
+
+
+def read_probe(buf, xor_out, threads_per_cta: int = 512, ctas_per_sm: int = 4, loads_in_flight: int = 8,
+               stream=None) -> None:
+    """Stream the whole contiguous device tensor ``buf`` once (c128_read_probe) and XOR its 32-bit
+    words into the int32 device tensor ``xor_out`` (one element, zero it first)."""
+    if not buf.is_contiguous():
+        raise ValueError("read_probe needs a contiguous tensor")
+    nbytes = buf.numel() * buf.element_size()
+    _check(lib().c128_read_probe(buf.data_ptr(), nbytes, int(threads_per_cta), int(ctas_per_sm),
+                                 int(loads_in_flight), xor_out.data_ptr(), _stream_handle(stream)),
+           "c128_read_probe")
 
 
 def release_all() -> None:

@@ -17,7 +17,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libc128compress.so")
-SOURCES = ["c128_kernels.cu", "c128_gather.cu", "c128_c4.cu", "c128_indexer.cu", "c128_api.cu", "c128_noalloc.cu"]
+SOURCES = ["c128_kernels.cu", "c128_gather.cu", "c128_c4.cu", "c128_indexer.cu", "c128_api.cu", "c128_noalloc.cu",
+           "c128_probe.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -337,6 +337,23 @@ typedef struct c128_info {
 } c128_info_t;
 int c128_get_info(c128_info_t* info);
 
+/* Read-bandwidth probe (a measurement helper; the pages have no counterpart). It streams `bytes`
+ * of the device buffer `buf` once with plain 16-byte loads and XORs every 32-bit word into the
+ * device word *xor_out (atomicXor per warp: zero it first and it ends as the XOR of the buffer's
+ * words, which proves every byte was read). The compressor's kernels read far more than they
+ * write, so this read rate, taken in the same process, is the denominator beside the copy
+ * bandwidth for their reported bandwidth fraction.
+ *   threads_per_cta   32..1024, a multiple of 32
+ *   ctas_per_sm       1..32, with threads_per_cta x ctas_per_sm <= 2048; the grid is #SM x the
+ *                     smaller of ctas_per_sm and the CTAs that fit on an SM at once (so all are
+ *                     resident), fewer when the buffer holds less than one load per thread
+ *   loads_in_flight   16-byte loads each thread issues before it uses them: 1, 2, 4 or 8
+ * `buf` 16-byte aligned, `bytes` a multiple of 16; both pointers are caller-owned device memory
+ * and nothing is allocated. Stream-ordered and asynchronous. Returns C128_ERR_ARG (bad sizes or
+ * launch shape), C128_ERR_NULL_PTR, C128_ERR_ALIGN or C128_ERR_CUDA; bytes == 0 is a no-op. */
+int c128_read_probe(const void* buf, int64_t bytes, int32_t threads_per_cta, int32_t ctas_per_sm,
+                    int32_t loads_in_flight, uint32_t* xor_out, c128_stream_t stream);
+
 /* Free every workspace and timer the library holds (synchronises the device). */
 int c128_release_all(void);
 

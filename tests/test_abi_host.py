@@ -268,3 +268,27 @@ def test_ex_validation_codes(L, case, code):
     elif case == "mxfp4_stride_odd":
         a.update(cfg=binding.config(128, 4, 1, 256, 2), kc=_t([4, 1, 69], U8), bs=1)
     assert _call_ex(L, a) == code
+
+
+# ------------------------------------------------------------------ read-bandwidth probe (host side)
+@pytest.mark.parametrize("args,code", [
+    ((FAKE, 24, 512, 2, 8), 7),         # bytes not a multiple of 16
+    ((FAKE, -16, 512, 2, 8), 7),        # negative size
+    ((FAKE, 64, 48, 2, 8), 7),          # threads not a multiple of 32
+    ((FAKE, 64, 2048, 1, 8), 7),        # threads above 1024
+    ((FAKE, 64, 1024, 3, 8), 7),        # more than 2048 threads per SM
+    ((FAKE, 64, 512, 0, 8), 7),         # no CTA per SM
+    ((FAKE, 64, 512, 2, 16), 7),        # loads in flight outside 1, 2, 4, 8
+    ((FAKE, 64, 512, 2, 3), 7),
+    ((0, 64, 512, 2, 8), 1),            # NULL buffer
+    ((FAKE + 8, 64, 512, 2, 8), 5),     # buffer not 16-byte aligned
+    ((0, 0, 512, 2, 8), 0),             # empty: no-op, nothing touched
+])
+def test_read_probe_validation(L, args, code):
+    buf, nbytes, threads, ctas, loads = args
+    assert L.c128_read_probe(buf, nbytes, threads, ctas, loads, FAKE, None) == code
+
+
+def test_read_probe_null_result_word(L):
+    assert L.c128_read_probe(FAKE, 64, 512, 2, 8, None, None) == 1
+    assert L.c128_read_probe(FAKE, 64, 512, 2, 8, FAKE + 2, None) == 5
