@@ -4,8 +4,9 @@
 //   warp 0      scheduler: claims 32 windows at a time; one lane per window resolves the token's
 //               request, position, cache slot and state blocks, checks them, and writes the
 //               resolved windows into a queue of two batches.
-//   warp 1      copier: takes the queued windows in order, one window per lane, gives each the
-//               next stage of the ring once the stage is free, writes the stage's descriptor and
+//   warp 1      copier: lane l takes the queued windows l, l + S, ... of each batch (S stages),
+//               each on the stage it maps to; the warp polls its lanes' stages together, so a
+//               lane issues as soon as its own stage is free. It writes the stage's descriptor and
 //               issues the copies: one tiled TMA load (`cp.async.bulk.tensor.5d`) per group of
 //               `ratio` consecutive rows (the older and the newer half of an overlapping window),
 //               whose box takes the kv half-row and the score half-row of every row of the group;
@@ -50,6 +51,9 @@ constexpr int kBatch = 32;  // windows claimed at once
 #endif
 #ifndef C128_SMALL_STAGES_128
 #define C128_SMALL_STAGES_128 24
+#endif
+#ifndef C128_C4_POLL_NS
+#define C128_C4_POLL_NS 64  // the copier's back-off when none of its lanes could issue
 #endif
 constexpr int kFlagTiled = 1;  // the state map serves the row copies
 
@@ -144,6 +148,19 @@ __device__ __forceinline__ void tma_load_5d(void* dst, const CUtensorMap* map, i
       "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4), "r"(smem_addr(bar)),
       "l"(policy)
       : "memory");
+}
+
+// Non-blocking test of a phase: true once the phase with this parity has completed.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred P;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 P, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, P;\n}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
 }
 
 __device__ __forceinline__ void set_timeout(const Params& p, int* abort_flag) {
@@ -314,8 +331,8 @@ __device__ void small_copier(const Params& p, SmallSmem<HEAD>& S, int lane, cons
   const bool joined = p.sw == HEAD;  // the score half-row follows the kv half-row: one copy per row
   uint32_t k = 0;                    // windows given a stage so far
   bool failed = false;
-  int pass_slot = -1;                // this lane's stage in the pass that failed, if it issued copies
-  uint32_t pass_k = 0;
+  int pass_slot = -1;                // the stage of this lane's last window in the batch that failed,
+  uint32_t pass_k = 0;               // if it issued copies, and that window
   for (uint32_t b = 0; !failed; ++b) {
     const int qs = b & 1;
     bool ok = mbar_wait_suspend(&S.qfull[qs], (b >> 1) & 1u, abort_flag);
@@ -325,62 +342,80 @@ __device__ void small_copier(const Params& p, SmallSmem<HEAD>& S, int lane, cons
     }
     const int n = S.qcount[qs];
     if (n < 0) break;
-    // passes of at most kStages windows: distinct stages, one lane each
-    for (int i0 = 0; i0 < n; i0 += G::kStages) {
-      const int j = i0 + lane;
-      const uint32_t kk = k + lane;
+    // Lane l < kStages takes the batch's windows j = l, l + kStages, ... (< n) in order; window j
+    // is window k + j overall and goes to stage (k + j) % kStages, which last held window
+    // k + j - kStages (same group) and is free once that group released it. The warp polls the
+    // lanes' stages together and each lane issues its next window as soon as its own stage is free
+    // (a blocking wait per lane would hold every lane until the last stage of the batch is free).
+    int j = lane;
+    bool pending = lane < G::kStages && j < n;
+    ok = true;
+    uint64_t t_progress = global_timer_ns();
+    for (;;) {
+      const uint32_t kk = k + static_cast<uint32_t>(j);
       const int sl = kk % G::kStages;
-      ok = true;
-      if (lane < G::kStages && j < n) {
-        // stage sl last held window kk - kStages (same group); it is free once that group released it
-        if (kk >= static_cast<uint32_t>(G::kStages))
-          ok = mbar_wait_suspend(&S.empty[sl], ((kk / G::kStages) - 1u) & 1u, abort_flag);
-        if (ok) {
-          const SmallDesc& e = S.queue[qs][j];
-          SmallDesc& d = S.desc[sl];
-          const int nvalid = e.nvalid;
-          d.tok = e.tok;
-          d.scale = e.scale;
-          d.cs_row = e.cs_row;
-          d.comp_dst = e.comp_dst;
-          d.nvalid = nvalid;
-          if (nvalid < 0) {
-            mbar_arrive(&S.full[sl]);  // nothing to copy: the group skips the window
+      const bool ready = pending && (kk < static_cast<uint32_t>(G::kStages) ||
+                                     mbar_test_wait(&S.empty[sl], ((kk / G::kStages) - 1u) & 1u));
+      if (ready) {
+        const SmallDesc& e = S.queue[qs][j];
+        SmallDesc& d = S.desc[sl];
+        const int nvalid = e.nvalid;
+        d.tok = e.tok;
+        d.scale = e.scale;
+        d.cs_row = e.cs_row;
+        d.comp_dst = e.comp_dst;
+        d.nvalid = nvalid;
+        if (nvalid < 0) {
+          mbar_arrive(&S.full[sl]);  // nothing to copy: the group skips the window
+        } else {
+          // the arrival releases the descriptor to the group that waits on this stage
+          mbar_arrive_expect_tx(&S.full[sl], static_cast<uint32_t>(nvalid * G::kRowFloats * 4));
+          pass_slot = sl;
+          pass_k = kk;
+          float* st = S.stage[sl];
+          if (e.stall) {
+            // test of the bounded waits: this stage never fills, so its group gives up after the
+            // time limit and the kernel reports C128_DEV_TIMEOUT instead of hanging
+          } else if (tiled) {
+            // box {cw, head/cw, 2, ratio, 1}: per row the kv half-row, then the score half-row
+            const int ng = e.ngroups;
+            for (int g = 0; g < ng; ++g)
+              tma_load_5d(st + g * p.ratio * G::kRowFloats, map, 0, e.g_half[g] * (HEAD / kCw), 0, e.g_row[g],
+                          e.g_blk[g], &S.full[sl], policy);
+          } else if (joined) {
+            for (int i = 0; i < nvalid; ++i)
+              bulk_copy_g2s(st + i * G::kRowFloats, e.row[i], G::kRowFloats * 4, &S.full[sl], policy);
           } else {
-            // the arrival releases the descriptor to the group that waits on this stage
-            mbar_arrive_expect_tx(&S.full[sl], static_cast<uint32_t>(nvalid * G::kRowFloats * 4));
-            pass_slot = sl;
-            pass_k = kk;
-            float* st = S.stage[sl];
-            if (e.stall) {
-              // test of the bounded waits: this stage never fills, so its group gives up after the
-              // time limit and the kernel reports C128_DEV_TIMEOUT instead of hanging
-            } else if (tiled) {
-              // box {cw, head/cw, 2, ratio, 1}: per row the kv half-row, then the score half-row
-              const int ng = e.ngroups;
-              for (int g = 0; g < ng; ++g)
-                tma_load_5d(st + g * p.ratio * G::kRowFloats, map, 0, e.g_half[g] * (HEAD / kCw), 0, e.g_row[g],
-                            e.g_blk[g], &S.full[sl], policy);
-            } else if (joined) {
-              for (int i = 0; i < nvalid; ++i)
-                bulk_copy_g2s(st + i * G::kRowFloats, e.row[i], G::kRowFloats * 4, &S.full[sl], policy);
-            } else {
-              for (int i = 0; i < nvalid; ++i) {
-                bulk_copy_g2s(st + i * G::kRowFloats, e.row[i], HEAD * 4, &S.full[sl], policy);
-                bulk_copy_g2s(st + i * G::kRowFloats + HEAD, e.row[i] + p.sw, HEAD * 4, &S.full[sl], policy);
-              }
+            for (int i = 0; i < nvalid; ++i) {
+              bulk_copy_g2s(st + i * G::kRowFloats, e.row[i], HEAD * 4, &S.full[sl], policy);
+              bulk_copy_g2s(st + i * G::kRowFloats + HEAD, e.row[i] + p.sw, HEAD * 4, &S.full[sl], policy);
             }
           }
         }
+        j += G::kStages;
+        pending = j < n;
       }
-      if (!__all_sync(0xffffffffu, ok)) {
-        failed = true;
-        break;
+      if (__ballot_sync(0xffffffffu, pending) == 0u) break;
+      const uint64_t now = global_timer_ns();
+      if (__any_sync(0xffffffffu, ready)) {
+        t_progress = now;
+      } else {
+        if (__any_sync(0xffffffffu, *abort_flag != 0) ||
+            __shfl_sync(0xffffffffu, now - t_progress > kWaitTimeoutNs ? 1 : 0, 0)) {
+          ok = !pending;
+          break;
+        }
+#if C128_C4_POLL_NS > 0
+        __nanosleep(C128_C4_POLL_NS);
+#endif
       }
-      pass_slot = -1;
-      k += min(G::kStages, n - i0);
     }
-    if (failed) break;
+    if (!__all_sync(0xffffffffu, ok)) {
+      failed = true;
+      break;
+    }
+    pass_slot = -1;
+    k += static_cast<uint32_t>(n);
     mbar_arrive(&S.qempty[qs]);  // the batch's entries were copied into the stage descriptors
   }
   if (!failed) {
@@ -400,8 +435,8 @@ __device__ void small_copier(const Params& p, SmallSmem<HEAD>& S, int lane, cons
   }
   if (failed) {
     if (lane == 0) set_timeout(p, &S.abort_flag);
-    // let every copy this warp issued land before the CTA may exit: the windows of earlier passes
-    // still in their stages, and this lane's window of the failed pass
+    // let every copy this warp issued land before the CTA may exit: the windows of earlier batches
+    // still in their stages, and this lane's last window of the batch that failed
     if (lane == 0)
       for (uint32_t j = k > static_cast<uint32_t>(G::kStages) ? k - G::kStages : 0u; j < k; ++j)
         mbar_wait(&S.full[j % G::kStages], (j / G::kStages) & 1u, nullptr);
