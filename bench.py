@@ -422,13 +422,14 @@ def sweep(args, dev):
     """µs per call vs token_num. Before every timed call a 512 MB buffer is written (L2 flush); the
     flush, the events and the call are enqueued back to back and synchronised once per size, so
     host launch time hides behind the flush. Columns: eager calls, CUDA-graph replays of the same
-    call, the pages' method (four input sets in rotation, back to back, no flush), and a cold
-    rotation (enough state sets that four times L2 separates two uses of one set, no flush)."""
+    call, the pages' method (four input sets in rotation, back to back, no flush), a cold
+    rotation (enough state sets that four times L2 separates two uses of one set, no flush), and
+    L2-hot (one input set, back to back, no flush: what fits in L2 is read from it)."""
     import torch
     from deepseek_v4_sparse_c128_gb300 import binding
     flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
     l2 = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 129 * 1024 * 1024))
-    eager, graph, rot4, cold = {}, {}, {}, {}
+    eager, graph, rot4, cold, hot = {}, {}, {}, {}, {}
     for T in inputs.SWEEP_TOKENS:
         p = inputs.make_problem("sweep", tokens=T, state_device=str(dev))
         to = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
@@ -447,6 +448,14 @@ def sweep(args, dev):
             with torch.cuda.graph(g, stream=s):
                 call()
             n = 50 if T < 4096 else 20
+            # L2-hot: the same call back to back, no flush
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(s)
+            for _ in range(4 * n):
+                call()
+            b.record(s)
+            s.synchronize()
+            hot[str(T)] = round(a.elapsed_time(b) * 1e3 / (4 * n), 3)
             # the pages' method (PR #44230, Performance: bench_inputs=4): four input sets used in
             # rotation, no flush in between, so small sizes partly hit L2
             sets = [call]
@@ -502,7 +511,8 @@ def sweep(args, dev):
                 (eager if mode == "eager" else graph)[str(T)] = round(us, 3)
             assert binding.device_errors(s, clear=True) == 0
         del d, p, g, call
-    return {"eager": eager, "graph": graph, "rotate4_no_flush": rot4, "rotate_cold_no_flush": cold}
+    return {"eager": eager, "graph": graph, "rotate4_no_flush": rot4, "rotate_cold_no_flush": cold,
+            "l2_hot_same_inputs": hot}
 
 
 def next_algorithmic_bytes(p, pos):
