@@ -5,7 +5,8 @@
   rows and nothing may overflow;
 - scores offset by +1e4 or -1e4 per state block: large magnitudes, where within a window the
   blocks with the lower offset get weights that underflow to 0.
-Each on every C128 call path (cluster split, token striding, planning pass)."""
+Each on every C128 call path (cluster split, token striding, planning pass); and -inf scores in
+the four other configurations."""
 import numpy as np
 import pytest
 
@@ -47,3 +48,24 @@ def test_extreme_scores(T, kind):
     rep = check_against_oracle(p, kc, comp, threads=16)
     assert rep["stored"] == T
     assert np.isfinite(comp[np.isfinite(comp[:, 0])]).all()
+
+
+@pytest.mark.parametrize("name", ["c4_sparse", "idx_c4_fp8", "idx_c4_mxfp4", "idx_c128_fp8"])
+def test_neg_inf_scores_other_configurations(name):
+    """-inf scores on random columns of random rows, except the last row of every group of
+    `ratio` positions, so every window keeps a finite score in each column (with overlap the older
+    group's last row is the finite one of its half)."""
+    from gpu_util import check_against_oracle_ex, run_gpu_ex
+    p = inputs.make_next_problem(name, scale=1)
+    rng = np.random.default_rng(len(name))
+    sw, sb = p.state_width, p.state.shape[1]
+    for r in range(p.block_table.shape[0]):
+        qs = p.positions[p.token_to_req == r]
+        for q in qs[(qs >= 0) & (qs % p.ratio != p.ratio - 1)]:
+            if rng.random() < 0.3:
+                cols = rng.random(sw) < 0.5
+                p.state[p.block_table[r, q // sb], q % sb, sw:][cols] = -np.inf
+    kc, comp, err = run_gpu_ex(p)
+    assert err == 0
+    rep = check_against_oracle_ex(p, kc, comp)
+    assert rep["stored"] > 0
