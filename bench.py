@@ -637,6 +637,24 @@ def run_case(args):
     build.build()
     binding.load()
     dev = torch.device("cuda", 0)
+    if args.case == "read_probe":
+        # the read probe alone over a 1 GiB buffer (8x L2), in the shape that led the bench's sweep
+        buf = torch.randint(-2**31, 2**31 - 1, (1 << 28,), dtype=torch.int32, device=dev)
+        word = torch.zeros(1, dtype=torch.int32, device=dev)
+        stream = torch.cuda.current_stream()
+        run = lambda: binding.read_probe(buf, word, 512, 4, 4, stream=stream)
+        for _ in range(args.warmup):
+            run()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(args.steps):
+            run()
+        b.record(stream)
+        torch.cuda.synchronize()
+        us = a.elapsed_time(b) * 1e3 / max(args.steps, 1)
+        print(json.dumps({"case": args.case, "bytes": buf.numel() * 4, "calls": args.steps, "us_per_call": us,
+                          "gbs": buf.numel() * 4 / (us * 1e-6) / 1e9, "device_errors": 0}), flush=True)
+        return
     if args.case == "sweep":
         p = inputs.make_problem("sweep", tokens=args.tokens, state_device=str(dev))
         cfg = None
@@ -679,7 +697,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-next", action="store_true")
     ap.add_argument("--no-read-probe", action="store_true")
-    ap.add_argument("--case", choices=["sweep"] + list(NEXT_SCALES),
+    ap.add_argument("--case", choices=["sweep", "read_probe"] + list(NEXT_SCALES),
                     help="run one workload alone (no JSON bench line); used for profiling")
     args = ap.parse_args()
     if args.case:
