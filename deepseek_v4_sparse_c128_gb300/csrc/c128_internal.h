@@ -78,10 +78,11 @@ struct Params {
                               // small-window kernel)
 };
 
-// True for the configuration the specialised C128 kernels serve.
+// True for the configurations the specialised C128 kernels serve: the C128 layout, with 8-row
+// state blocks or, through the configurable entry point, any multiple of 8 rows.
 inline bool is_c128(const Params& p) {
   return p.head == kHead && p.ratio == kRatio && p.overlap == 0 && p.sw == kHead && p.fmt == 0 &&
-         p.sblk == kStateBlock;
+         p.sblk >= kStateBlock && p.sblk % kStateBlock == 0;
 }
 
 struct LaunchCfg {

@@ -66,8 +66,22 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(Params p) {
 }
 
 // --------------------------------------------------------------------------- compress kernel
+// State blocks other than 8 rows (any multiple of 8, through the configurable entry point): the
+// window's 128 rows are 16 chunks of 8 rows, chunk j starting at row q0 = start + 8j of the
+// request, which is row q0 % sblk of block block_table[req][q0 / sblk]. start is a multiple of 128
+// and sblk of 8, so a chunk never spans two blocks. Returns the block id (for the range check)
+// and the chunk's element offset. The 8-row kernels (the C128 layout, where a chunk is a block)
+// are separate template instances that carry none of these 64-bit divisions.
+__device__ __forceinline__ int chunk_block(const Params& p, int req, long long start, int j, int64_t* off) {
+  const long long q0 = start + static_cast<long long>(kStateBlock) * j;
+  const long long col = q0 / p.sblk, row = q0 - col * p.sblk;
+  const int blk = __ldg(p.bt + static_cast<int64_t>(req) * p.bt_stride + col);
+  *off = static_cast<int64_t>(blk) * p.s0 + row * p.s1;
+  return blk;
+}
+
 struct __align__(16) WinDesc {
-  const float* src[kWindowBlocks];  // row 0 of each of the window's 16 state blocks
+  const float* src[kWindowBlocks];  // first row of each of the window's 16 chunks of 8 rows
   uint8_t* kv_dst;                  // 576 token bytes of the k_cache slot
   uint8_t* scale_dst;               // 8 scale bytes of the slot
   const float* cs_row;              // cos_sin_cache row of the window start
@@ -88,6 +102,7 @@ struct Smem {
   int abort_flag;
 };
 
+template <bool ANY>
 __device__ void scheduler_warp(const Params& p, Smem& S, int lane) {
   const bool strided = p.strided != 0;
   if (!strided) grid_dependency_wait();  // the list and the counters come from plan_kernel
@@ -148,7 +163,7 @@ __device__ void scheduler_warp(const Params& p, Smem& S, int lane) {
           kvs = __ldg(p.kvslot + t);
         }
         if (req < 0 || req >= p.bt_rows) err |= C128_DEV_BAD_REQ;
-        if (pos / kStateBlock >= p.bt_cols) err |= C128_DEV_BAD_BT_COL;
+        if ((ANY ? pos / p.sblk : pos / kStateBlock) >= p.bt_cols) err |= C128_DEV_BAD_BT_COL;
         if (pos - (kRatio - 1) >= p.cs_rows) err |= C128_DEV_BAD_COS_ROW;  // (p/128)*128 == p-127
         if (kvs >= p.nkb * p.kv_bs) err |= C128_DEV_BAD_KV_SLOT;
       }
@@ -159,9 +174,14 @@ __device__ void scheduler_warp(const Params& p, Smem& S, int lane) {
       err = __shfl_sync(0xffffffffu, err, 0);
     }
     int blk = 0;
+    int64_t choff = 0;
     if (!end && !(err & (C128_DEV_BAD_REQ | C128_DEV_BAD_BT_COL))) {
-      if (lane < kWindowBlocks)
-        blk = __ldg(p.bt + static_cast<int64_t>(req) * p.bt_stride + (pos - (kRatio - 1)) / kStateBlock + lane);
+      if constexpr (ANY) {
+        if (lane < kWindowBlocks) blk = chunk_block(p, req, pos - (kRatio - 1), lane, &choff);
+      } else {
+        if (lane < kWindowBlocks)
+          blk = __ldg(p.bt + static_cast<int64_t>(req) * p.bt_stride + (pos - (kRatio - 1)) / kStateBlock + lane);
+      }
       const bool bad = lane < kWindowBlocks && (blk < 0 || blk >= p.nb);
       if (__any_sync(0xffffffffu, bad)) err |= C128_DEV_BAD_BLOCK;
     }
@@ -183,7 +203,7 @@ __device__ void scheduler_warp(const Params& p, Smem& S, int lane) {
     }
     WinDesc& d = S.desc[ds];
     if (!end) {
-      if (lane < kWindowBlocks) d.src[lane] = p.state + static_cast<int64_t>(blk) * p.s0;
+      if (lane < kWindowBlocks) d.src[lane] = p.state + (ANY ? choff : static_cast<int64_t>(blk) * p.s0);
       if (lane == 0) {
         const long long kb = kvs / p.kv_bs, off = kvs % p.kv_bs;
         uint8_t* base = p.kc + kb * p.kc_stride0;
@@ -311,6 +331,7 @@ __device__ void consumer_warps(const Params& p, Smem& S, int ci) {
   }
 }
 
+template <bool ANY>
 __global__ void __launch_bounds__(kThreads, 1) compress_kernel(Params p) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
   Smem& S = *reinterpret_cast<Smem*>(smem_raw);
@@ -329,7 +350,7 @@ __global__ void __launch_bounds__(kThreads, 1) compress_kernel(Params p) {
   }
   __syncthreads();
   if (warp == 0) {
-    scheduler_warp(p, S, lane);
+    scheduler_warp<ANY>(p, S, lane);
   } else if (warp == 1) {
     if (lane == 0) copy_thread(p, S);
   } else {
@@ -387,7 +408,7 @@ __device__ __forceinline__ int ld_cluster_s32(uint32_t addr) {
   return v;
 }
 
-template <int S>
+template <int S, bool ANY>
 __global__ void __launch_bounds__(kThreads, 1) direct_kernel(Params p) {
   using Cfg = DirectCfg<S>;
   extern __shared__ __align__(128) unsigned char smem_raw[];
@@ -415,13 +436,18 @@ __global__ void __launch_bounds__(kThreads, 1) direct_kernel(Params p) {
   if (!((slot >= 0) & (pos >= 0) & ((pos & (kRatio - 1)) == kRatio - 1) & (kvs >= 0))) return;
   uint32_t err = 0;
   if (req < 0 || req >= p.bt_rows) err |= C128_DEV_BAD_REQ;
-  if (pos / kStateBlock >= p.bt_cols) err |= C128_DEV_BAD_BT_COL;
+  if ((ANY ? pos / p.sblk : pos / kStateBlock) >= p.bt_cols) err |= C128_DEV_BAD_BT_COL;
   if (pos - (kRatio - 1) >= p.cs_rows) err |= C128_DEV_BAD_COS_ROW;
   if (kvs >= p.nkb * p.kv_bs) err |= C128_DEV_BAD_KV_SLOT;
-  int blk = 0;  // lane j of every warp holds block id j of the window
+  int blk = 0;  // lane j of every warp holds the block id of chunk j
   if (!(err & (C128_DEV_BAD_REQ | C128_DEV_BAD_BT_COL))) {
-    if (lane < kWindowBlocks)
-      blk = __ldg(p.bt + static_cast<int64_t>(req) * p.bt_stride + (pos - (kRatio - 1)) / kStateBlock + lane);
+    if constexpr (ANY) {
+      int64_t unused;
+      if (lane < kWindowBlocks) blk = chunk_block(p, req, pos - (kRatio - 1), lane, &unused);
+    } else {
+      if (lane < kWindowBlocks)
+        blk = __ldg(p.bt + static_cast<int64_t>(req) * p.bt_stride + (pos - (kRatio - 1)) / kStateBlock + lane);
+    }
     if (__any_sync(0xffffffffu, lane < kWindowBlocks && (blk < 0 || blk >= p.nb))) err |= C128_DEV_BAD_BLOCK;
   }
   if (err) {
@@ -439,6 +465,7 @@ __global__ void __launch_bounds__(kThreads, 1) direct_kernel(Params p) {
     uint32_t issued = 0;
     const uint64_t policy = l2_evict_first_policy();
     for (int j = 0; j < Cfg::kBlocks; ++j) {
+      // the block id travels by shuffle (32 bits), lane 0 adds the chunk's row within the block
       const int b = __shfl_sync(0xffffffffu, blk, static_cast<int>(rank) * Cfg::kBlocks + j);
       if (lane == 0 && !failed) {
         const int s = j % Cfg::kRing;
@@ -447,7 +474,11 @@ __global__ void __launch_bounds__(kThreads, 1) direct_kernel(Params p) {
           failed = true;
         } else {
           mbar_arrive_expect_tx(&D.full[s], kStageBytes);
-          const float* src = p.state + static_cast<int64_t>(b) * p.s0;
+          int64_t o = static_cast<int64_t>(b) * p.s0;
+          if constexpr (ANY)
+            o += ((pos - (kRatio - 1) + static_cast<long long>(kStateBlock) * (static_cast<int>(rank) * Cfg::kBlocks + j)) %
+                  p.sblk) * p.s1;
+          const float* src = p.state + o;
           if (p.s1 == kRow) {
             bulk_copy_g2s(D.stage[s], src, kStageBytes, &D.full[s], policy);
           } else {
@@ -553,7 +584,7 @@ int direct_split(int64_t T, int sm_count) {
   return 1;
 }
 
-template <int S>
+template <int S, bool ANY>
 cudaError_t launch_direct(const Params& p, const LaunchCfg& cfg, cudaStream_t stream) {
   if (cfg.ev_begin != nullptr) {
     const cudaError_t e = cudaEventRecord(cfg.ev_begin, stream);
@@ -571,7 +602,7 @@ cudaError_t launch_direct(const Params& p, const LaunchCfg& cfg, cudaStream_t st
   attr[0].val.clusterDim.z = 1;
   lc.attrs = attr;
   lc.numAttrs = S > 1 ? 1 : 0;
-  cudaError_t e = cudaLaunchKernelEx(&lc, direct_kernel<S>, p);
+  cudaError_t e = cudaLaunchKernelEx(&lc, direct_kernel<S, ANY>, p);
   if (e != cudaSuccess) return e;
   if (cfg.ev_end != nullptr) e = cudaEventRecord(cfg.ev_end, stream);
   return e;
@@ -581,13 +612,23 @@ cudaError_t launch_direct(const Params& p, const LaunchCfg& cfg, cudaStream_t st
 
 int compress_smem_bytes() { return static_cast<int>(sizeof(Smem)); }
 
+namespace {
+template <bool ANY>
+cudaError_t set_direct_smem(cudaFuncAttribute a) {
+  cudaError_t e = cudaFuncSetAttribute(direct_kernel<1, ANY>, a, static_cast<int>(sizeof(DirectSmem<1>)));
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(direct_kernel<2, ANY>, a, static_cast<int>(sizeof(DirectSmem<2>)));
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(direct_kernel<4, ANY>, a, static_cast<int>(sizeof(DirectSmem<4>)));
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(direct_kernel<8, ANY>, a, static_cast<int>(sizeof(DirectSmem<8>)));
+  return e;
+}
+}  // namespace
+
 cudaError_t prepare_device(int /*device*/) {
   const cudaFuncAttribute a = cudaFuncAttributeMaxDynamicSharedMemorySize;
-  cudaError_t e = cudaFuncSetAttribute(compress_kernel, a, static_cast<int>(sizeof(Smem)));
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(direct_kernel<1>, a, static_cast<int>(sizeof(DirectSmem<1>)));
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(direct_kernel<2>, a, static_cast<int>(sizeof(DirectSmem<2>)));
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(direct_kernel<4>, a, static_cast<int>(sizeof(DirectSmem<4>)));
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(direct_kernel<8>, a, static_cast<int>(sizeof(DirectSmem<8>)));
+  cudaError_t e = cudaFuncSetAttribute(compress_kernel<false>, a, static_cast<int>(sizeof(Smem)));
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(compress_kernel<true>, a, static_cast<int>(sizeof(Smem)));
+  if (e == cudaSuccess) e = set_direct_smem<false>(a);
+  if (e == cudaSuccess) e = set_direct_smem<true>(a);
   if (e == cudaSuccess) e = prepare_small();
   if (e == cudaSuccess) e = prepare_indexer_windows();
   return e;
@@ -625,11 +666,12 @@ cudaError_t launch(const Params& p, const LaunchCfg& cfg, cudaStream_t stream) {
     if (cfg.ev_end != nullptr) e = cudaEventRecord(cfg.ev_end, stream);
     return e;
   }
+  const bool any_block = p.sblk != kStateBlock;  // the C128 layout has 8-row state blocks
   switch (direct_split(p.T, cfg.sm_count)) {
-    case 8: return launch_direct<8>(p, cfg, stream);
-    case 4: return launch_direct<4>(p, cfg, stream);
-    case 2: return launch_direct<2>(p, cfg, stream);
-    case 1: return launch_direct<1>(p, cfg, stream);
+    case 8: return any_block ? launch_direct<8, true>(p, cfg, stream) : launch_direct<8, false>(p, cfg, stream);
+    case 4: return any_block ? launch_direct<4, true>(p, cfg, stream) : launch_direct<4, false>(p, cfg, stream);
+    case 2: return any_block ? launch_direct<2, true>(p, cfg, stream) : launch_direct<2, false>(p, cfg, stream);
+    case 1: return any_block ? launch_direct<1, true>(p, cfg, stream) : launch_direct<1, false>(p, cfg, stream);
     default: break;
   }
   cudaError_t e;
@@ -638,7 +680,10 @@ cudaError_t launch(const Params& p, const LaunchCfg& cfg, cudaStream_t stream) {
     Params q = p;
     q.strided = 1;
     if (cfg.ev_begin != nullptr && (e = cudaEventRecord(cfg.ev_begin, stream)) != cudaSuccess) return e;
-    compress_kernel<<<cfg.grid, kThreads, sizeof(Smem), stream>>>(q);
+    if (any_block)
+      compress_kernel<true><<<cfg.grid, kThreads, sizeof(Smem), stream>>>(q);
+    else
+      compress_kernel<false><<<cfg.grid, kThreads, sizeof(Smem), stream>>>(q);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (cfg.ev_end != nullptr) e = cudaEventRecord(cfg.ev_end, stream);
     return e;
@@ -660,7 +705,7 @@ cudaError_t launch(const Params& p, const LaunchCfg& cfg, cudaStream_t stream) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   lc.attrs = attr;
   lc.numAttrs = (cfg.pdl && cfg.ev_begin == nullptr) ? 1 : 0;
-  e = cudaLaunchKernelEx(&lc, compress_kernel, p);
+  e = any_block ? cudaLaunchKernelEx(&lc, compress_kernel<true>, p) : cudaLaunchKernelEx(&lc, compress_kernel<false>, p);
   if (e != cudaSuccess) return e;
   if (cfg.ev_end != nullptr) e = cudaEventRecord(cfg.ev_end, stream);
   return e;

@@ -64,11 +64,34 @@ def test_c128_config_through_ex_is_the_c128_call():
         assert np.array_equal(ca[rows].view(np.uint32), cb[rows].view(np.uint32))
 
 
-def test_c128_config_with_other_block_size_uses_generic_path():
-    """C128 sizes with a state block of 16 rows: the generic kernel, checked against the oracle."""
-    p = inputs.prefill_problem("c128b16", 5, 3, 128, 3000, 512, 128, 0, 0, state_block=16, decode_tail=20)
+@pytest.mark.parametrize("sblk", [16, 24, 64, 128, 256, 12, 20])
+@pytest.mark.parametrize("shape", ["direct", "striding", "planned"])
+def test_c128_config_with_other_block_sizes(sblk, shape):
+    """C128 sizes with state blocks other than 8 rows: multiples of 8 take the C128 kernels (a
+    window's 8-row chunks sit at row q0 % sblk of block q0 / sblk), others the generic kernel; each
+    launch mode of the C128 kernels (cluster split up to #SM tokens, token striding up to 8 per SM,
+    then the planning pass), checked against the oracle."""
+    reqs, lo, hi = {"direct": (1, 128, 128), "striding": (1, 600, 600), "planned": (3, 128, 3000)}[shape]
+    p = inputs.prefill_problem(f"c128b{sblk}", 5 + sblk, reqs, lo, hi, 512, 128, 0, 0, state_block=sblk,
+                               decode_tail=20)
     kc, comp, err = run_gpu_ex(p)
     assert err == 0
+    rep = check_against_oracle_ex(p, kc, comp, threads=16)
+    assert rep["stored"] > 0
+
+
+def test_c128_config_other_block_size_bad_indices():
+    """16-row state blocks on the C128 kernels: an out-of-range block id (BAD_BLOCK) and a window
+    end past the block table (BAD_BT_COL) are reported and skipped like with 8-row blocks."""
+    p = inputs.prefill_problem("c128b16bad", 9, 2, 1000, 2000, 512, 128, 0, 0, state_block=16, decode_tail=40)
+    act = np.nonzero((p.positions + 1) % 128 == 0)[0]
+    t1, t2 = int(act[3]), int(act[-2])
+    r1 = int(p.token_to_req[t1])
+    p.block_table[r1, (int(p.positions[t1]) - 127) // 16 + 3] = p.state.shape[0]   # BAD_BLOCK
+    p.positions[t2] = p.block_table.shape[1] * 16 + 127                             # BAD_BT_COL
+    kc, comp, err = run_gpu_ex(p)
+    ref = p.k_cache.copy()
+    assert err == oracle.forward_ex(p, k_cache=ref) and err & (2 | 4) == (2 | 4)
     check_against_oracle_ex(p, kc, comp, threads=16)
 
 
