@@ -245,13 +245,15 @@ int c128_compress_norm_rope_store_noalloc(const c128_tensor_t* token_to_req_indi
  * the indexer FP8 format and 2 for MXFP4 (the widest store of each), which the natural layout
  * bs x record bytes always is.
  * Everything else is as for compress_norm_rope_store; the C128 configuration (512, 64, 128, 0, 512,
- * sparse, state block 8) runs the same kernels as compress_norm_rope_store.
+ * sparse) runs the same kernels as compress_norm_rope_store when its state block is any multiple
+ * of 8 rows.
  * Returns C128_ERR_NULL_PTR for a NULL config and C128_ERR_UNSUPPORTED for a configuration outside
  * the ones above (another head or rope size, a head that does not match the format, a ratio that
  * is not a power of two or makes windows longer than 256 rows, overlap other than 0 or 1, a state
  * width below (1 + overlap) * head_dim or not a multiple of 4); the tensor checks and their codes
  * are those of compress_norm_rope_store, with head_dim in place of 512.
- * Kernels: windows of at most 8 rows stream through a shared-memory ring (many windows per SM);
+ * Kernels: the C128 configuration with a state block that is a multiple of 8 rows runs the C128
+ * kernels; windows of at most 8 rows stream through a shared-memory ring (many windows per SM);
  * longer head-128 windows whose state block is a multiple of 8 rows stream in 8-row tiled loads;
  * the rest run a gather kernel. All of them are CUDA-graph capturable.
  */
