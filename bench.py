@@ -659,7 +659,7 @@ def run_case(args):
         p = inputs.make_problem("sweep", tokens=args.tokens, state_device=str(dev))
         cfg = None
     else:
-        p = inputs.make_next_problem(args.case, state_device=str(dev), scale=NEXT_SCALES[args.case])
+        p = inputs.make_next_problem(args.case, state_device=str(dev), scale=args.scale or NEXT_SCALES[args.case])
         cfg = binding.config(p.head, p.ratio, p.overlap, p.state_width, p.fmt)
     to = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
     d = {k: to(getattr(p, k)) for k in ("token_to_req", "positions", "slot_mapping", "block_table", "rms_w",
@@ -679,8 +679,13 @@ def run_case(args):
     b.record(stream)
     torch.cuda.synchronize()
     errs = binding.device_errors(clear=True)
-    print(json.dumps({"case": args.case, "tokens": p.num_tokens, "calls": args.steps,
-                      "us_per_call": a.elapsed_time(b) * 1e3 / max(args.steps, 1), "device_errors": errs}), flush=True)
+    us = a.elapsed_time(b) * 1e3 / max(args.steps, 1)
+    out = {"case": args.case, "tokens": p.num_tokens, "calls": args.steps, "us_per_call": us, "device_errors": errs}
+    if args.case != "sweep":
+        active = (p.positions >= 0) & ((p.positions + 1) % p.ratio == 0)   # every token here has a slot
+        out.update(windows=int(active.sum()),
+                   algorithmic_gbs=round(next_algorithmic_bytes(p, p.positions[active]) / (us * 1e-6) / 1e9, 1))
+    print(json.dumps(out), flush=True)
     if errs:
         raise SystemExit(1)
 
@@ -697,6 +702,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-next", action="store_true")
     ap.add_argument("--no-read-probe", action="store_true")
+    ap.add_argument("--scale", type=int, default=None,
+                    help="with --case and another configuration: request-count scale (default: the bench size)")
     ap.add_argument("--case", choices=["sweep", "read_probe"] + list(NEXT_SCALES),
                     help="run one workload alone (no JSON bench line); used for profiling")
     args = ap.parse_args()
