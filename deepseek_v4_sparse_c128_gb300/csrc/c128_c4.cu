@@ -325,7 +325,7 @@ template <int HEAD>
 __device__ void small_copier(const Params& p, SmallSmem<HEAD>& S, int lane, const CUtensorMap* map, bool tiled) {
   using G = SmallGeo<HEAD>;
   constexpr int kCw = HEAD < 256 ? HEAD : 256;
-  static_assert(G::kStages <= 32 && G::kGroups <= G::kStages, "one lane per window of a pass");
+  static_assert(G::kStages <= 32 && G::kGroups <= G::kStages, "one copier lane per stage, one end marker per group");
   const volatile int* abort_flag = &S.abort_flag;
   const uint64_t policy = l2_evict_first_policy();
   const bool joined = p.sw == HEAD;  // the score half-row follows the kv half-row: one copy per row
