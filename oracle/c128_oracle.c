@@ -13,15 +13,28 @@
  * "FP8 UE8M0 quant", "GPT-J RoPE"), and vLLM PR #44230 (Summary: head 512, state width 512,
  * compress ratio 128, no overlap, state block 8).
  *
- * Readings taken where the pages leave a step open (every one is listed in the design notes):
- *   - positions < 0 are inactive (the pages' modulo would call p = -1 a window end);
- *   - softmax and weighted sum are evaluated in binary64 and rounded once to fp32 (comp32);
- *   - variance = RN32( exact(sum c^2) / 512 ), the sum taken exactly (big-integer accumulator);
- *   - rrms = the correctly rounded fp32 1/sqrt(RN32(var + eps)) (computed in binary64);
- *   - every other fp32 product / sum is one IEEE fp32 operation, left to right, no FMA;
- *   - fp32 -> bf16 and fp32 -> e4m3 round to nearest, ties to even; e4m3 saturates at 448
- *     and keeps the sign (so -0 and negative underflow give 0x80);
- *   - the UE8M0 exponent is the exact ceil(log2(raw)), raw = RN32(absmax * RN32(1/448)).
+ * Readings taken where the pages leave a step open. The fused kernel's listing on the API page
+ * states the operations in Triton (`%`, tl.softmax, tl.sum, tl.rsqrt, .to(bfloat16) and
+ * .to(float8e4nv)) but not their precision, rounding or evaluation order, so:
+ *   - positions < 0 are inactive: the page's window-end test uses a modulo under which p = -1
+ *     would count as a window end whose rows are all masked ("Gather state cache entries",
+ *     mask_pos = pos >= 0), a window with no row to weight;
+ *   - softmax and weighted sum ("Gather state cache entries", tl.softmax then tl.sum) are
+ *     evaluated in binary64 and rounded once to fp32 (comp32); their summation order is free,
+ *     and the GPU is held to a tolerance on comp32, not to its bits;
+ *   - variance = RN32( exact(sum c^2) / 512 ) ("RMSNorm": tl.sum of the squares over HEAD_SIZE),
+ *     the sum taken exactly (big-integer accumulator) so that its order cannot matter;
+ *   - rrms = the correctly rounded fp32 1/sqrt(RN32(var + eps)) (tl.rsqrt's accuracy is not
+ *     stated; the correctly rounded value is the one precision-free reading), computed in binary64;
+ *   - every other fp32 product / sum is one IEEE fp32 operation, left to right as printed
+ *     ("RMSNorm": compressed_kv * rrms * rms_w; "GPT-J RoPE": even*cos - odd*sin), no FMA;
+ *   - fp32 -> bf16 and fp32 -> e4m3 round to nearest, ties to even (the casts' default mode);
+ *     e4m3 saturates at FP8_MAX = 448 after the page's clamp and keeps the sign (so -0 and
+ *     negative underflow give 0x80);
+ *   - the UE8M0 exponent is the exact ceil(log2(raw)), raw = RN32(absmax * RN32(1/448))
+ *     ("FP8 UE8M0 quant" multiplies by the reciprocal and takes ceil of log2; for every
+ *     positive bf16 absmax at or above the 1e-4 floor the exact and the approximate log2 give the
+ *     same integer, so the exact one is used).
  *
  * Build: cc -O2 -ffp-contract=off -fPIC -shared c128_oracle.c -lm
  */
@@ -319,8 +332,11 @@ typedef struct c128o_cfg {
 
 /* E2M1 (OCP MXFP4 element): sign, 2 exponent bits (bias 1), 1 mantissa bit; magnitudes
  * 0, 0.5, 1, 1.5, 2, 3, 4, 6. Nearest by exhaustive search, ties to the even code, values beyond
- * 6 saturate, the sign bit of x is kept. (The page's _fp32x2_to_fp4x2 body is not printed; this
- * round-to-nearest-even, saturating reading is the one the design notes list.) */
+ * 6 saturate, the sign bit of x is kept. The API page calls a helper _fp32x2_to_fp4x2 on the
+ * scaled pairs of _fused_kv_compress_norm_rope_insert_indexer_mxfp4_attn but does not print its
+ * body, so the rounding is a reading: round to nearest with ties to the even code (the OCP
+ * microscaling convention for conversions into E2M1) and saturation at 6, the largest
+ * magnitude, because the block scale is chosen so that |x| * 2^-e <= 6 up to rounding. */
 uint8_t c128o_e2m1(float x) {
     static const double mag[8] = {0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0};
     double a = fabs((double)x);
