@@ -17,7 +17,7 @@ C128_I32, C128_I64, C128_F32, C128_U8 = 1, 2, 3, 4
 STATUS = {
     0: "C128_OK", 1: "C128_ERR_NULL_PTR", 2: "C128_ERR_DTYPE", 3: "C128_ERR_SHAPE", 4: "C128_ERR_STRIDE",
     5: "C128_ERR_ALIGN", 6: "C128_ERR_UNSUPPORTED", 7: "C128_ERR_ARG", 8: "C128_ERR_CUDA", 9: "C128_ERR_NOMEM",
-    10: "C128_ERR_TOO_MANY_TOKENS",
+    10: "C128_ERR_TOO_MANY_TOKENS", 11: "C128_ERR_CAPTURE",
 }
 NOALLOC_MAX_TOKENS = 65536  # C128_NOALLOC_MAX_TOKENS
 DEV_BITS = {1: "BAD_REQ", 2: "BAD_BT_COL", 4: "BAD_BLOCK", 8: "BAD_COS_ROW", 16: "BAD_KV_SLOT", 32: "TIMEOUT"}
@@ -32,6 +32,7 @@ EXPORTS = (
     "c128_debug_stall_first_window_ex",
     "c128_status_string",
     "c128_reserve_workspace",
+    "c128_release_stream",
     "c128_device_errors",
     "c128_kernel_timer_begin",
     "c128_kernel_timer_end",
@@ -102,6 +103,7 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     L.c128_status_string.argtypes = [ctypes.c_int]
     L.c128_status_string.restype = ctypes.c_char_p
     L.c128_reserve_workspace.argtypes = [i64, vp]
+    L.c128_release_stream.argtypes = [vp]
     L.c128_device_errors.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32), ctypes.c_int]
     L.c128_kernel_timer_begin.argtypes = [vp]
     L.c128_kernel_timer_end.argtypes = [vp, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int64)]
@@ -293,6 +295,11 @@ def call_status(*args, **kw) -> int:
 
 def reserve_workspace(max_tokens: int, stream=None) -> None:
     _check(lib().c128_reserve_workspace(int(max_tokens), _stream_handle(stream)), "c128_reserve_workspace")
+
+
+def release_stream(stream=None) -> None:
+    """Return the stream's workspace and timer events (stream-ordered; before destroying it)."""
+    _check(lib().c128_release_stream(_stream_handle(stream)), "c128_release_stream")
 
 
 def device_errors(stream=None, clear: bool = True) -> int:

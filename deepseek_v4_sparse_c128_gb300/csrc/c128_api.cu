@@ -55,33 +55,40 @@ int device_info(int dev, DeviceInfo** out) {
   return C128_OK;
 }
 
-// Must hold g_mu. Ensure the (dev, stream) workspace holds `tokens` list entries.
+// Must hold g_mu. Ensure the (dev, stream) workspace holds `tokens` list entries. Growth is
+// stream-ordered and never waits on the host: the new buffer comes from the device's default
+// memory pool (cudaMallocAsync on `stream`), the 256-byte header moves over with a device-to-device
+// copy on `stream` (so the sticky error bits survive), and the old buffer goes back to the pool
+// with cudaFreeAsync on `stream`, after every earlier call on the stream has used it. A stream
+// that is being captured cannot grow its workspace: the call returns C128_ERR_CAPTURE.
 int workspace_for(int dev, cudaStream_t stream, int64_t tokens, WsHeader** out) {
   Workspace& w = g_ws[{dev, stream}];
   if (w.ptr != nullptr && w.capacity >= tokens) {
     *out = w.ptr;
     return C128_OK;
   }
+  cudaStreamCaptureStatus cap_status = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &cap_status) != cudaSuccess) {
+    cudaGetLastError();
+    return C128_ERR_CUDA;
+  }
+  if (cap_status != cudaStreamCaptureStatusNone) return C128_ERR_CAPTURE;
   int64_t cap = w.capacity > 0 ? w.capacity : 4096;
   while (cap < tokens) cap *= 2;
-  WsHeader old{};
-  if (w.ptr != nullptr) {  // keep the sticky error bits of the old workspace
-    if (cudaStreamSynchronize(stream) != cudaSuccess) return C128_ERR_CUDA;
-    if (cudaMemcpy(&old, w.ptr, sizeof(old), cudaMemcpyDeviceToHost) != cudaSuccess) return C128_ERR_CUDA;
-    cudaFree(w.ptr);
-    w.ptr = nullptr;
-    w.capacity = 0;
-  }
   void* p = nullptr;
-  if (cudaMalloc(&p, sizeof(WsHeader) + static_cast<size_t>(cap) * sizeof(int32_t)) != cudaSuccess) {
+  if (cudaMallocAsync(&p, sizeof(WsHeader) + static_cast<size_t>(cap) * sizeof(int32_t), stream) != cudaSuccess) {
     cudaGetLastError();
     return C128_ERR_NOMEM;
   }
-  WsHeader h{};
-  h.err = old.err;
-  if (cudaMemcpy(p, &h, sizeof(h), cudaMemcpyHostToDevice) != cudaSuccess) {
-    cudaFree(p);
+  const cudaError_t e = w.ptr != nullptr
+                            ? cudaMemcpyAsync(p, w.ptr, sizeof(WsHeader), cudaMemcpyDeviceToDevice, stream)
+                            : cudaMemsetAsync(p, 0, sizeof(WsHeader), stream);
+  if (e != cudaSuccess) {
+    cudaFreeAsync(p, stream);
     return C128_ERR_CUDA;
+  }
+  if (w.ptr != nullptr && cudaFreeAsync(w.ptr, stream) != cudaSuccess) {
+    cudaGetLastError();  // the old buffer stays allocated; the new one is in use from here on
   }
   w.ptr = static_cast<WsHeader*>(p);
   w.capacity = cap;
@@ -369,6 +376,9 @@ const char* c128_status_string(int status) {
     case C128_ERR_ARG: return "bad argument (kv_block_size must equal k_cache.shape[1]; too many tokens)";
     case C128_ERR_CUDA: return "CUDA error";
     case C128_ERR_NOMEM: return "workspace allocation failed";
+    case C128_ERR_CAPTURE:
+      return "the stream's workspace would have to grow while the stream is being captured "
+             "(call c128_reserve_workspace with the largest batch before capturing)";
     case C128_ERR_TOO_MANY_TOKENS:
       return "more tokens than the static workspace of c128_compress_norm_rope_store_noalloc holds "
              "(C128_NOALLOC_MAX_TOKENS)";
@@ -462,21 +472,61 @@ int c128_get_info(c128_info_t* info) {
   return C128_OK;
 }
 
+int c128_release_stream(c128_stream_t stream) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return C128_ERR_CUDA;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaStreamCaptureStatus cap_status = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(s, &cap_status) != cudaSuccess) {
+    cudaGetLastError();
+    return C128_ERR_CUDA;
+  }
+  if (cap_status != cudaStreamCaptureStatusNone) return C128_ERR_CAPTURE;  // a free would join the graph
+  std::lock_guard<std::mutex> lk(g_mu);
+  int rc = C128_OK;
+  auto it = g_ws.find({dev, s});
+  if (it != g_ws.end()) {
+    if (it->second.ptr != nullptr && cudaFreeAsync(it->second.ptr, s) != cudaSuccess) {
+      cudaGetLastError();
+      rc = C128_ERR_CUDA;
+    }
+    g_ws.erase(it);
+  }
+  auto tt = g_timers.find({dev, s});
+  if (tt != g_timers.end()) {
+    for (auto& ev : tt->second.events) {  // destruction waits for pending records by itself
+      cudaEventDestroy(ev.first);
+      cudaEventDestroy(ev.second);
+    }
+    g_timers.erase(tt);
+  }
+  return rc;
+}
+
 int c128_release_all(void) {
   std::lock_guard<std::mutex> lk(g_mu);
-  if (!g_ws.empty() || !g_timers.empty()) {
-    if (cudaDeviceSynchronize() != cudaSuccess) return C128_ERR_CUDA;
+  int cur = 0;
+  if (cudaGetDevice(&cur) != cudaSuccess) return C128_ERR_CUDA;
+  int rc = C128_OK;
+  for (auto& kv : g_ws) {
+    if (kv.second.ptr == nullptr) continue;
+    // the buffer came from the pool of device kv.first.first: free it there, after all work
+    if (cudaSetDevice(kv.first.first) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess ||
+        cudaFreeAsync(kv.second.ptr, 0) != cudaSuccess || cudaStreamSynchronize(0) != cudaSuccess) {
+      cudaGetLastError();
+      rc = C128_ERR_CUDA;
+    }
   }
-  for (auto& kv : g_ws)
-    if (kv.second.ptr) cudaFree(kv.second.ptr);
   g_ws.clear();
+  if (!g_timers.empty() && cudaDeviceSynchronize() != cudaSuccess) rc = C128_ERR_CUDA;
   for (auto& kv : g_timers)
     for (auto& ev : kv.second.events) {
       cudaEventDestroy(ev.first);
       cudaEventDestroy(ev.second);
     }
   g_timers.clear();
-  return C128_OK;
+  if (cudaSetDevice(cur) != cudaSuccess) rc = C128_ERR_CUDA;
+  return rc;
 }
 
 }  // extern "C"

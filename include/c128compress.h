@@ -32,13 +32,21 @@
  * 576 token bytes and 8 scale bytes of an active token's slot is touched.
  *
  * All tensors are caller-owned device memory described by c128_tensor_t (strides in elements).
- * The call is asynchronous on `stream` (no host synchronisation, no device-to-host read).
- * It uses a per-(device, stream) workspace owned by the library: the first call on a stream, and
- * any call with more tokens than that workspace holds, allocates it with cudaMalloc (call
- * c128_reserve_workspace first to keep later calls, for example under CUDA-graph capture, free
- * of allocation). Calls on the same stream are serialised by the stream; calls on different
- * streams use different workspaces. Two active tokens naming the same kv slot race (undefined
- * which one lands); this is not checked.
+ * The call is asynchronous on `stream`: it never synchronises the host with the GPU and never
+ * reads device memory back to the host.
+ * It uses a per-(device, stream) workspace owned by the library (a 256-byte header with the
+ * sticky device error bits, then one int32 per token). The first call on a stream, and any call
+ * with more tokens than that workspace holds, grows it stream-ordered: a new buffer from the
+ * device's default memory pool (cudaMallocAsync on `stream`), the header copied device-to-device
+ * on `stream`, the old buffer returned with cudaFreeAsync on `stream`. Nothing waits on the host.
+ * A stream that is being captured into a CUDA graph cannot grow its workspace: such a call
+ * returns C128_ERR_CAPTURE and enqueues nothing, so call c128_reserve_workspace with the largest
+ * batch before capturing. A graph keeps the workspace it was captured with; a later call on the
+ * same stream that grows the workspace frees that buffer, so reserve enough before capturing a
+ * graph that will be replayed. Calls on the same stream are serialised by the stream; calls on
+ * different streams use different workspaces. c128_release_stream returns one stream's workspace
+ * (call it before destroying the stream). Two active tokens naming the same kv slot race
+ * (undefined which one lands); this is not checked.
  */
 #ifndef C128COMPRESS_H
 #define C128COMPRESS_H
@@ -70,7 +78,8 @@ typedef struct c128_tensor {
 } c128_tensor_t;
 
 /* Return codes. Every error is detected on the host before anything is launched, except
- * C128_ERR_CUDA (a CUDA call or launch failed) and C128_ERR_NOMEM (workspace allocation). */
+ * C128_ERR_CUDA (a CUDA call or launch failed) and C128_ERR_NOMEM (workspace allocation);
+ * C128_ERR_CAPTURE is also returned before anything is enqueued. */
 enum {
     C128_OK = 0,
     C128_ERR_NULL_PTR = 1,     /* a descriptor, or the data of a non-empty tensor, is NULL */
@@ -83,6 +92,7 @@ enum {
     C128_ERR_CUDA = 8,
     C128_ERR_NOMEM = 9,
     C128_ERR_TOO_MANY_TOKENS = 10, /* c128_compress_norm_rope_store_noalloc: T > C128_NOALLOC_MAX_TOKENS */
+    C128_ERR_CAPTURE = 11,     /* the stream is being captured and its workspace would have to grow */
 };
 
 /* Device-side error bits (OR-ed into the stream's workspace, sticky until cleared).
@@ -311,9 +321,19 @@ int c128_debug_stall_first_window_ex(const c128_config_t* config,
 /* Human-readable name of a return code (static string, never NULL). */
 const char* c128_status_string(int status);
 
-/* Make the workspace of (current device, stream) hold at least max_tokens tokens. May call
- * cudaMalloc/cudaFree (and synchronise the stream when it replaces a smaller workspace). */
+/* Make the workspace of (current device, stream) hold at least max_tokens tokens, growing it
+ * stream-ordered as described at the top (cudaMallocAsync / device-to-device header copy /
+ * cudaFreeAsync on `stream`, no host synchronisation). Returns C128_ERR_CAPTURE if it would have
+ * to grow while `stream` is being captured, C128_ERR_NOMEM if the pool has no room. */
 int c128_reserve_workspace(int64_t max_tokens, c128_stream_t stream);
+
+/* Return the workspace and kernel-timer events of (current device, stream) to the library: the
+ * workspace is freed with cudaFreeAsync on `stream`, after the work already enqueued there, and
+ * the stream's sticky device error bits go with it. Call it before destroying a stream the
+ * library was used on (a later call on a stream with the same handle starts a fresh workspace).
+ * Does not synchronise. Returns C128_ERR_CAPTURE (and releases nothing) while `stream` is being
+ * captured. */
+int c128_release_stream(c128_stream_t stream);
 
 /* Synchronise `stream`, store the device error bits (C128_DEV_*) of its workspace in *bits,
  * and clear them when `clear` is non-zero. A stream never used reports 0. */
@@ -356,7 +376,8 @@ int c128_get_info(c128_info_t* info);
 int c128_read_probe(const void* buf, int64_t bytes, int32_t threads_per_cta, int32_t ctas_per_sm,
                     int32_t loads_in_flight, uint32_t* xor_out, c128_stream_t stream);
 
-/* Free every workspace and timer the library holds (synchronises the device). */
+/* Free every workspace and timer the library holds, on every device it was used on
+ * (synchronises those devices). */
 int c128_release_all(void);
 
 #ifdef __cplusplus

@@ -66,3 +66,29 @@ def test_noalloc_refuses_batches_beyond_its_static_array(binding):
     assert e.value.status == 10
     torch.cuda.synchronize()
     assert np.array_equal(d["k_cache"].cpu().numpy(), p.k_cache)
+
+
+def test_noalloc_allocates_nothing_and_covers_token_striding(binding):
+    """After one warm-up call (the first call on a device loads the library's static array and
+    looks up its address), two more calls on a stream the allocating entry point never used leave
+    the device's free memory and torch's reserved memory exactly as they were. The batch has twice
+    as many tokens as the GPU has SMs, which runs the compress kernel in token-striding mode."""
+    import torch
+    sm = torch.cuda.get_device_properties(0).multi_processor_count
+    p = inputs.make_problem("sweep", tokens=2 * sm)
+    ref, new, warm = _device(p), _device(p), _device(p)
+    binding.compress_norm_rope_store(*_args(p, ref))
+    binding.compress_norm_rope_store_noalloc(*_args(p, warm))
+    torch.cuda.synchronize()
+    want = ref["k_cache"].cpu().numpy()
+    assert np.array_equal(warm["k_cache"].cpu().numpy(), want)
+    s = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    free0, reserved0 = torch.cuda.mem_get_info()[0], torch.cuda.memory_reserved()
+    for _ in range(2):
+        binding.compress_norm_rope_store_noalloc(*_args(p, new), stream=s)
+    torch.cuda.synchronize()
+    free1, reserved1 = torch.cuda.mem_get_info()[0], torch.cuda.memory_reserved()
+    assert free1 == free0, f"device free memory changed by {free1 - free0} bytes"
+    assert reserved1 == reserved0
+    assert np.array_equal(new["k_cache"].cpu().numpy(), want)
