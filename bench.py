@@ -218,15 +218,16 @@ def run_ours(args, ws, rank, local):
         # ten equal chunks of the timed steps, each between two events on the stream, for min/median
         chunk = args.steps // 10 if args.steps >= 10 else args.steps
         marks = []
-        with binding.KernelTimer() as ktimer:
-            e0.record(stream)
-            for i in range(args.steps):
-                if i % chunk == 0 and len(marks) < args.steps // chunk:
-                    marks.append((i, torch.cuda.Event(enable_timing=True)))
-                    marks[-1][1].record(stream)
-                step()
-            e1.record(stream)
-            torch.cuda.synchronize()
+        # the calls exactly as a caller makes them: no kernel timer, so the planning kernel and the
+        # compress kernel overlap through programmatic dependent launch
+        e0.record(stream)
+        for i in range(args.steps):
+            if i % chunk == 0 and len(marks) < args.steps // chunk:
+                marks.append((i, torch.cuda.Event(enable_timing=True)))
+                marks[-1][1].record(stream)
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
         barrier(ws)
     local_ms = e0.elapsed_time(e1)
     ends = marks[1:] + [(args.steps, e1)]
@@ -235,6 +236,14 @@ def run_ours(args, ws, rank, local):
     max_ms, total_windows = reduce_max_sum(ws, local_ms, float(T * args.steps))
     value = total_windows / (max_ms / 1e3)
     ms_per_step = max_ms / args.steps
+    # the compress kernel alone, in a separate pass after the timed region: the library's kernel
+    # timer records events around it (which turns programmatic dependent launch off for these calls)
+    timer_calls = max(3, min(args.steps, 200))
+    with binding.KernelTimer() as ktimer:
+        for _ in range(timer_calls):
+            step()
+        torch.cuda.synchronize()
+    assert binding.device_errors(clear=True) == 0, "device error in the kernel-timer pass"
     kernel_ms = ktimer.total_ms / max(1, ktimer.launches)
 
     # ---- end to end through the public API: every step uploads its token metadata and block table
@@ -322,6 +331,8 @@ def run_ours(args, ws, rank, local):
     out["roofline"] = {"bound": "hbm", "kernel": "compress_kernel", "achieved": achieved, "peak": peak,
                        "peak_source": peak_src, "unit": "GB/s", "frac": achieved / peak,
                        "traffic": traffic_per_launch(T), "kernel_us": kernel_ms * 1e3,
+                       "kernel_us_from": f"library kernel timer (CUDA events on the stream around the compress "
+                                         f"kernel), {ktimer.launches} calls after the timed region",
                        "algorithmic_bytes_per_launch": T * ALGO_BYTES_PER_WINDOW}
     out["clocks"] = clocks.summary()
     if not args.no_read_probe:
@@ -344,6 +355,8 @@ def run_ours(args, ws, rank, local):
                                          f"({cpu_s:.1f} s CPU), oracle over host threads",
                                "single_thread": {"value": wps1, "unit": UNIT, "cores": 1,
                                                  "sample": f"128 of those windows x {passes1} passes"}}
+    if not args.no_workloads and ws == 1:
+        out["workloads"] = bench_workloads(args, dev, peak, out.get("hbm_read_probe", {}).get("gbs"))
     if not args.no_next and ws == 1:
         out["other_configurations"] = bench_next(args, dev)
     if not args.no_sweep and ws == 1:
@@ -441,21 +454,21 @@ def sweep(args, dev):
             call = binding.PreparedCall(d["token_to_req"], d["positions"], d["slot_mapping"], d["block_table"],
                                         p.state, d["rms_w"], p.eps, d["cos_sin"], d["k_cache"], d["kv_slot_mapping"],
                                         p.kv_block_size, stream=s)
-            for _ in range(5):
+            for _ in range(args.sweep_warmup):
                 call()
             s.synchronize()
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=s):
                 call()
-            n = 50 if T < 4096 else 20
+            n = args.sweep_calls
             # L2-hot: the same call back to back, no flush
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(s)
-            for _ in range(4 * n):
+            for _ in range(n):
                 call()
             b.record(s)
             s.synchronize()
-            hot[str(T)] = round(a.elapsed_time(b) * 1e3 / (4 * n), 3)
+            hot[str(T)] = round(a.elapsed_time(b) * 1e3 / n, 3)
             # the pages' method (PR #44230, Performance: bench_inputs=4): four input sets used in
             # rotation, no flush in between, so small sizes partly hit L2
             sets = [call]
@@ -466,15 +479,15 @@ def sweep(args, dev):
                 sets.append(binding.PreparedCall(dk["token_to_req"], dk["positions"], dk["slot_mapping"],
                                                  dk["block_table"], st_k, dk["rms_w"], p.eps, dk["cos_sin"],
                                                  dk["k_cache"], dk["kv_slot_mapping"], p.kv_block_size, stream=s))
-            for c in sets:
-                c()
+            for i in range(max(4, args.sweep_warmup)):
+                sets[i % 4]()
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(s)
-            for i in range(4 * n):
+            for i in range(n):
                 sets[i % 4]()
             b.record(s)
             s.synchronize()
-            rot4[str(T)] = round(a.elapsed_time(b) * 1e3 / (4 * n), 3)
+            rot4[str(T)] = round(a.elapsed_time(b) * 1e3 / n, 3)
             del sets
             # cold rotation: R = max(4, ceil(4 L2 / state bytes per call)) state sets cycled, no flush,
             # so every call reads state that is not in L2 and nothing dirty is left to write back
@@ -487,15 +500,15 @@ def sweep(args, dev):
                 sets = [binding.PreparedCall(d["token_to_req"], d["positions"], d["slot_mapping"], d["block_table"],
                                              big[k * nb:(k + 1) * nb], d["rms_w"], p.eps, d["cos_sin"], d["k_cache"],
                                              d["kv_slot_mapping"], p.kv_block_size, stream=s) for k in range(R)]
-                for c in sets:
-                    c()
+                for i in range(max(R, args.sweep_warmup)):
+                    sets[i % R]()
                 a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 a.record(s)
-                for i in range(4 * n):
+                for i in range(n):
                     sets[i % R]()
                 b.record(s)
                 s.synchronize()
-                cold[str(T)] = round(a.elapsed_time(b) * 1e3 / (4 * n), 3)
+                cold[str(T)] = round(a.elapsed_time(b) * 1e3 / n, 3)
                 del sets, big
             for mode, fn in (("eager", call), ("graph", g.replay)):
                 evs = []
@@ -512,7 +525,10 @@ def sweep(args, dev):
             assert binding.device_errors(s, clear=True) == 0
         del d, p, g, call
     return {"eager": eager, "graph": graph, "rotate4_no_flush": rot4, "rotate_cold_no_flush": cold,
-            "l2_hot_same_inputs": hot}
+            "l2_hot_same_inputs": hot,
+            "timing": f"{args.sweep_warmup} warm-up calls, then {args.sweep_calls} timed calls per column and "
+                      f"token_num (mean; CUDA events around the timed calls, or around each call in the flush "
+                      f"columns)"}
 
 
 def next_algorithmic_bytes(p, pos):
@@ -587,6 +603,97 @@ def bench_next(args, dev):
         rec = current_traffic_record(traffic.get(name)) if isinstance(traffic.get(name), dict) else None
         res[name]["ncu_dram_bytes_per_window"] = None if rec is None else rec["dram_bytes_per_window"]
         del d, p, call
+        torch.cuda.empty_cache()
+    return res
+
+
+WORKLOADS = ("tiny", "decode", "mixed", "varlen", "varlen16k")
+META_BYTES_PER_TOKEN = 4 + 8 + 8 + 8   # token_to_req (int32), positions, slot_mapping, kv_slot_mapping (int64)
+
+
+def active_windows(p) -> np.ndarray:
+    """Tokens that store a window: slot >= 0, position >= 0 at a window end, kv slot >= 0."""
+    return ((p.slot_mapping >= 0) & (p.positions >= 0) & ((p.positions + 1) % inputs.RATIO == 0)
+            & (p.kv_slot_mapping >= 0))
+
+
+def workload_bytes(p) -> int:
+    """Algorithmic bytes of one call: 525,192 per active window (its 128 state rows, 16 block ids,
+    the cos/sin row and the 584-byte slot) + 28 per token of metadata + the 2 KiB RMSNorm weight."""
+    return int(active_windows(p).sum()) * ALGO_BYTES_PER_WINDOW + META_BYTES_PER_TOKEN * p.num_tokens + 4 * 512
+
+
+def bench_workloads(args, dev, peak: float, probe_gbs):
+    """The five synthetic workloads (tiny, decode, mixed, varlen, varlen16k) through the public call:
+    µs per call (mean of the timed calls, and min / median over ten chunks of them), compressed
+    windows/s, algorithmic GB/s and its fraction of the measured copy bandwidth and of the read
+    probe, in two columns: cold (R state sets in rotation, R x state bytes >= 4 x L2, so no call
+    finds its state in L2) and L2-hot (one input set back to back). Beside them, the CPU oracle
+    over all host threads on the same workload (state copied to the host)."""
+    import dataclasses
+    import torch
+    from deepseek_v4_sparse_c128_gb300 import binding
+    import oracle
+    l2 = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 129 * 1024 * 1024))
+    threads = os.cpu_count() or 1
+    oracle.build()
+    res = {}
+    for name in WORKLOADS:
+        p = inputs.make_problem(name, state_device=str(dev))
+        to = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+        d = {k: to(getattr(p, k)) for k in ("token_to_req", "positions", "slot_mapping", "block_table", "rms_w",
+                                            "cos_sin", "k_cache", "kv_slot_mapping")}
+        A = int(active_windows(p).sum())
+        nbytes = workload_bytes(p)
+        state_bytes = p.state.numel() * 4
+        R = max(1, -(-4 * l2 // state_bytes))
+        states = [p.state] + [inputs.draw_state(7000 + 31 * k + inputs.CONFIG_SEEDS[name], p.state.shape[0], str(dev))
+                              for k in range(1, R)]
+        s = torch.cuda.Stream(device=dev)
+        binding.reserve_workspace(p.num_tokens, s)
+        calls = [binding.PreparedCall(d["token_to_req"], d["positions"], d["slot_mapping"], d["block_table"], st,
+                                      d["rms_w"], p.eps, d["cos_sin"], d["k_cache"], d["kv_slot_mapping"],
+                                      p.kv_block_size, stream=s) for st in states]
+        n = args.workload_calls
+        row = {"tokens": p.num_tokens, "windows": A, "algorithmic_bytes_per_call": nbytes,
+               "state_sets": R, "state_bytes_per_set": state_bytes}
+        for col, rot in (("cold", len(calls)), ("l2_hot", 1)):
+            for i in range(max(50, rot)):
+                calls[i % rot]()
+            chunk = max(1, n // 10)
+            evs = [torch.cuda.Event(enable_timing=True) for _ in range(n // chunk + 1)]
+            evs[0].record(s)
+            for i in range(n // chunk * chunk):
+                calls[i % rot]()
+                if (i + 1) % chunk == 0:
+                    evs[(i + 1) // chunk].record(s)
+            s.synchronize()
+            per = [evs[k].elapsed_time(evs[k + 1]) * 1e3 / chunk for k in range(len(evs) - 1)]
+            us = evs[0].elapsed_time(evs[-1]) * 1e3 / (chunk * len(per))
+            gbs = nbytes / (us * 1e-6) / 1e9
+            row[col] = {"us_per_call": round(us, 3), "us_min_chunk": round(min(per), 3),
+                        "us_median_chunk": round(statistics.median(per), 3), "calls": chunk * len(per),
+                        "windows_per_s": A / (us * 1e-6), "algorithmic_gbs": round(gbs, 1),
+                        "frac_of_measured_hbm": round(gbs / peak, 3),
+                        "frac_of_read_probe": round(gbs / probe_gbs, 3) if probe_gbs else None}
+        assert binding.device_errors(s, clear=True) == 0, f"device error in workload {name}"
+        # the CPU oracle on the same workload (the first state set, copied to the host)
+        if not args.no_cpu_baseline:
+            host = dataclasses.replace(p, state=p.state.cpu().numpy())
+            passes, t0 = 0, time.perf_counter()
+            while True:
+                oracle.forward(host, k_cache=p.k_cache.copy(), threads=threads)
+                passes += 1
+                if time.perf_counter() - t0 > 1.0 or passes >= 20:
+                    break
+            wall = time.perf_counter() - t0
+            row["oracle"] = {"windows_per_s": A * passes / wall, "cores": threads, "passes": passes,
+                             "kind": "oracle", "sample": "the whole workload"}
+            del host
+        res[name] = row
+        s.synchronize()
+        binding.release_stream(s)
+        del calls, states, d, p
         torch.cuda.empty_cache()
     return res
 
@@ -702,6 +809,11 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-next", action="store_true")
     ap.add_argument("--no-read-probe", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true")
+    ap.add_argument("--sweep-warmup", type=int, default=50, help="warm-up calls per token_num of the sweep")
+    ap.add_argument("--sweep-calls", type=int, default=1000, help="timed calls per token_num and column")
+    ap.add_argument("--workload-calls", type=int, default=1000,
+                    help="timed calls per workload in the five-workload table")
     ap.add_argument("--scale", type=int, default=None,
                     help="with --case and another configuration: request-count scale (default: the bench size)")
     ap.add_argument("--case", choices=["sweep", "read_probe"] + list(NEXT_SCALES),

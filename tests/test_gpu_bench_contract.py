@@ -15,7 +15,7 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 def test_bench_json_line():
     cmd = [sys.executable, "bench.py", "--tokens", "2048", "--steps", "5", "--warmup", "3", "--no-sweep", "--no-next",
-           "--no-cpu-baseline"]
+           "--no-cpu-baseline", "--workload-calls", "20"]
     r = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=600)
     assert r.returncode == 0, r.stderr[-2000:]
     lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
@@ -38,3 +38,15 @@ def test_bench_json_line():
     assert d["gpu_launches"] == 2 * 5  # planning pass and compress kernel per step (2048 > 8 per SM)
     assert d["hbm_read_probe"]["gbs"] == rf["read_probe_gbs"] and d["hbm_read_probe"]["bytes"] > 0
     assert set(d["clocks"]) >= {"sm_mhz", "sm_max_mhz", "reasons"}
+    # the five synthetic workloads: windows/s = active windows / µs per call, GB/s = bytes / µs per call
+    w = d["workloads"]
+    assert set(w) == {"tiny", "decode", "mixed", "varlen", "varlen16k"}
+    assert [w[k]["windows"] for k in ("tiny", "decode")] == [4, 128]
+    for name, row in w.items():
+        assert row["windows"] > 0 and row["tokens"] >= row["windows"], name
+        for col in ("cold", "l2_hot"):
+            c = row[col]
+            assert c["calls"] == 20 and c["us_min_chunk"] <= c["us_median_chunk"], (name, col)
+            assert abs(c["windows_per_s"] - row["windows"] / (c["us_per_call"] * 1e-6)) <= 1e-3 * c["windows_per_s"]
+            gbs = row["algorithmic_bytes_per_call"] / (c["us_per_call"] * 1e-6) / 1e9
+            assert abs(c["algorithmic_gbs"] - gbs) <= 1e-3 * gbs + 0.1, (name, col)
