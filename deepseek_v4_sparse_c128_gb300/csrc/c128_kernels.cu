@@ -336,6 +336,12 @@ __global__ void __launch_bounds__(kThreads, 1) compress_kernel(Params p) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
   Smem& S = *reinterpret_cast<Smem*>(smem_raw);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // Token striding: launched as a programmatic dependent of the kernel before it on the stream
+  // (see direct_kernel). Planned path: a dependent of the planning kernel, whose results only the
+  // scheduler reads (after its own wait); what the other warps read was written before that
+  // kernel started.
+  launch_dependents();
+  if (p.strided) grid_dependency_wait();
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&S.full[s], 1);
@@ -416,6 +422,11 @@ __global__ void __launch_bounds__(kThreads, 1) direct_kernel(Params p) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t rank = S > 1 ? cluster_ctarank() : 0u;
   const int64_t t = static_cast<int64_t>(blockIdx.x) / S;
+  // Launched as a programmatic dependent of the kernel before it on the stream: the next call may
+  // start as soon as every CTA of this one runs, and this one reads nothing before the kernel
+  // before it has completed (its writes, possibly these inputs, are then visible).
+  launch_dependents();
+  grid_dependency_wait();
   // the token (every thread; broadcast loads), issued before the barrier set-up so that their
   // latency overlaps it
   const int64_t slot = __ldg(p.slot + t), pos = __ldg(p.pos + t), kvs = __ldg(p.kvslot + t);
@@ -595,13 +606,22 @@ cudaError_t launch_direct(const Params& p, const LaunchCfg& cfg, cudaStream_t st
   lc.blockDim = dim3(kThreads);
   lc.dynamicSmemBytes = sizeof(DirectSmem<S>);
   lc.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = S;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
+  cudaLaunchAttribute attr[2];
+  unsigned n = 0;
+  if (cfg.pdl && cfg.ev_begin == nullptr) {  // events between the kernels would serialise them anyway
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  if (S > 1) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = S;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
   lc.attrs = attr;
-  lc.numAttrs = S > 1 ? 1 : 0;
+  lc.numAttrs = n;
   cudaError_t e = cudaLaunchKernelEx(&lc, direct_kernel<S, ANY>, p);
   if (e != cudaSuccess) return e;
   if (cfg.ev_end != nullptr) e = cudaEventRecord(cfg.ev_end, stream);
@@ -680,11 +700,18 @@ cudaError_t launch(const Params& p, const LaunchCfg& cfg, cudaStream_t stream) {
     Params q = p;
     q.strided = 1;
     if (cfg.ev_begin != nullptr && (e = cudaEventRecord(cfg.ev_begin, stream)) != cudaSuccess) return e;
-    if (any_block)
-      compress_kernel<true><<<cfg.grid, kThreads, sizeof(Smem), stream>>>(q);
-    else
-      compress_kernel<false><<<cfg.grid, kThreads, sizeof(Smem), stream>>>(q);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = dim3(static_cast<unsigned>(cfg.grid));
+    lc.blockDim = dim3(kThreads);
+    lc.dynamicSmemBytes = sizeof(Smem);
+    lc.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    lc.attrs = attr;
+    lc.numAttrs = (cfg.pdl && cfg.ev_begin == nullptr) ? 1 : 0;
+    e = any_block ? cudaLaunchKernelEx(&lc, compress_kernel<true>, q) : cudaLaunchKernelEx(&lc, compress_kernel<false>, q);
+    if (e != cudaSuccess) return e;
     if (cfg.ev_end != nullptr) e = cudaEventRecord(cfg.ev_end, stream);
     return e;
   }
