@@ -656,6 +656,12 @@ __global__ void __launch_bounds__(SmallGeo<HEAD>::kThreads, 1)
   extern __shared__ __align__(128) unsigned char smem_raw[];
   SmallSmem<HEAD>& S = *reinterpret_cast<SmallSmem<HEAD>*>(smem_raw);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // Token striding: a programmatic dependent of the kernel before it on the stream, so nothing
+  // global is touched before that kernel has completed; the next call may launch as soon as every
+  // CTA of this one runs. Planned path: a dependent of the planning kernel, whose results only the
+  // scheduler reads (after its own wait).
+  launch_dependents();
+  if (p.strided) grid_dependency_wait();
   if (tid == 0) {
     for (int s = 0; s < G::kStages; ++s) {
       mbar_init(&S.full[s], 1);

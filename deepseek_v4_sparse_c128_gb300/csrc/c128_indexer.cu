@@ -437,6 +437,12 @@ __global__ void __launch_bounds__(kIxThreads, 1)
   extern __shared__ __align__(128) unsigned char smem_raw[];
   IxSmem& S = *reinterpret_cast<IxSmem*>(smem_raw);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // Token striding: a programmatic dependent of the kernel before it on the stream, so nothing
+  // global is touched before that kernel has completed; the next call may launch as soon as every
+  // CTA of this one runs. Planned path: a dependent of the planning kernel, whose results only the
+  // scheduler reads (after its own wait).
+  launch_dependents();
+  if (p.strided) grid_dependency_wait();
   if (tid == 0) {
     for (int s = 0; s < kIxStages; ++s) {
       mbar_init(&S.full[s], 1);

@@ -101,3 +101,31 @@ def test_two_calls_in_one_graph(binding, T):
     assert np.array_equal(d["k_cache"].cpu().numpy(), _alone(binding, p, d["state"]))
     s.synchronize()
     binding.release_stream(s)
+
+
+@pytest.mark.parametrize("head,ratio,overlap,fmt", [(512, 4, 1, 0), (128, 4, 1, 1), (128, 4, 1, 2), (128, 128, 0, 1)])
+def test_the_later_of_two_calls_lands_other_configurations(binding, head, ratio, overlap, fmt):
+    """The small-window and indexer kernels in their token-striding range (at most 8 tokens per
+    SM), launched the same way: two calls on the same slots back to back, the later one's bytes."""
+    import torch
+    p = inputs.prefill_problem("pdl", 3, 3, 5 if ratio == 4 else 128, 300 if ratio == 4 else 500, head, ratio,
+                               overlap, fmt)
+    assert p.num_tokens <= 8 * 148
+    cfg = binding.config(p.head, p.ratio, p.overlap, p.state_width, p.fmt)
+
+    def run(d, state, reps):
+        for _ in range(reps):
+            binding.compress_norm_rope_store_ex(cfg, *_args(p, d, state))
+
+    d = to_device(p)
+    other = torch.randn_like(d["state"])
+    for _ in range(3):
+        run(d, other, 1)
+        run(d, None, 1)
+    torch.cuda.synchronize()
+    assert binding.device_errors(clear=True) == 0
+    ref = to_device(p)
+    run(ref, None, 1)
+    torch.cuda.synchronize()
+    assert not np.array_equal(ref["k_cache"].cpu().numpy(), p.k_cache)
+    assert np.array_equal(d["k_cache"].cpu().numpy(), ref["k_cache"].cpu().numpy())
