@@ -267,7 +267,7 @@ int run(const c128_tensor_t* ttr, const c128_tensor_t* pos, const c128_tensor_t*
     std::lock_guard<std::mutex> lk(g_mu);
     DeviceInfo* di = nullptr;
     C128_TRY(device_info(dev, &di));
-    C128_TRY(workspace_for(dev, stream, T, &p.ws));
+    C128_TRY(workspace_for(dev, stream, c128::plan_list_entries(T), &p.ws));
     cfg.sm_count = di->sm_count;
     // the C128 stall test needs the compress kernel: batches of more tokens than SMs
     if (stall_test && config == nullptr && T <= di->sm_count) return C128_ERR_ARG;
@@ -394,7 +394,8 @@ int c128_reserve_workspace(int64_t max_tokens, c128_stream_t stream) {
   DeviceInfo* di = nullptr;
   C128_TRY(device_info(dev, &di));
   WsHeader* ws = nullptr;
-  return workspace_for(dev, reinterpret_cast<cudaStream_t>(stream), max_tokens > 0 ? max_tokens : 1, &ws);
+  return workspace_for(dev, reinterpret_cast<cudaStream_t>(stream), c128::plan_list_entries(max_tokens > 0 ? max_tokens : 1),
+                       &ws);
 }
 
 int c128_device_errors(c128_stream_t stream, uint32_t* bits, int clear) {

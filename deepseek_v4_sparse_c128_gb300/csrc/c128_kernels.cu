@@ -65,6 +65,54 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(Params p) {
     if ((flags >> i) & 1u) list[out++] = static_cast<int32_t>(base + i * kPlanThreads + tid);
 }
 
+// C128 planning pass: CTA c takes tokens [c * 2048, (c + 1) * 2048), writes its active tokens in
+// token order at list[c * 2048 ...] and their number at list[T + c], and CTA 0 zeroes the claim
+// counter. Every word it writes is overwritten by each call, so no zeroing pass precedes it, and
+// the list order does not depend on which CTA finishes first. It is launched as a programmatic
+// dependent of the kernel before it (the previous call's compress kernel still reads the list and
+// the claim counter until it completes): it waits for that kernel before any global access.
+__global__ void __launch_bounds__(kPlanThreads) plan_chunks_kernel(Params p) {
+  launch_dependents();
+  grid_dependency_wait();
+  __shared__ uint32_t warp_base[kPlanThreads / 32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t base = static_cast<int64_t>(blockIdx.x) * kPlanTokensPerCta;
+  if (blockIdx.x == 0 && tid == 0) p.ws->next = 0u;
+  // thread tid takes tokens base + 8 tid .. + 7, so that the list comes out in token order
+  uint32_t flags = 0;
+#pragma unroll
+  for (int i = 0; i < kPlanTokensPerThread; ++i) {
+    const int64_t t = base + static_cast<int64_t>(tid) * kPlanTokensPerThread + i;
+    if (t < p.T) {
+      const int64_t s = __ldg(p.slot + t), pos = __ldg(p.pos + t), kv = __ldg(p.kvslot + t);
+      const bool active = (s >= 0) & (pos >= 0) & (((pos + 1) & (p.ratio - 1)) == 0) & (kv >= 0);
+      flags |= static_cast<uint32_t>(active) << i;
+    }
+  }
+  const uint32_t n = __popc(flags);
+  uint32_t incl = n;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) warp_base[warp] = incl;
+  __syncthreads();
+  uint32_t out = incl - n, total = 0;
+#pragma unroll
+  for (int w = 0; w < kPlanThreads / 32; ++w) {
+    const uint32_t c = warp_base[w];
+    if (w < warp) out += c;
+    total += c;
+  }
+  int32_t* list = reinterpret_cast<int32_t*>(p.ws + 1);
+#pragma unroll
+  for (int i = 0; i < kPlanTokensPerThread; ++i)
+    if ((flags >> i) & 1u)
+      list[base + out++] = static_cast<int32_t>(base + static_cast<int64_t>(tid) * kPlanTokensPerThread + i);
+  if (tid == 0) list[p.T + blockIdx.x] = static_cast<int32_t>(total);
+}
+
 // --------------------------------------------------------------------------- compress kernel
 // State blocks other than 8 rows (any multiple of 8, through the configurable entry point): the
 // window's 128 rows are 16 chunks of 8 rows, chunk j starting at row q0 = start + 8j of the
@@ -99,17 +147,34 @@ struct Smem {
   uint64_t dfull[kDescSlots];    // window descriptor written (scheduler)
   uint64_t dempty[kDescSlots];   // descriptor released (copy warp + consumer warps)
   EpiSmem epi;
+  uint32_t chunk_prefix[kMaxPlanChunks + 1];  // planned path: active windows before each chunk
   int abort_flag;
 };
 
 template <bool ANY>
 __device__ void scheduler_warp(const Params& p, Smem& S, int lane) {
   const bool strided = p.strided != 0;
-  if (!strided) grid_dependency_wait();  // the list and the counters come from plan_kernel
   const int32_t* list = reinterpret_cast<const int32_t*>(p.ws + 1);
   const volatile int* abort_flag = &S.abort_flag;
-  const uint32_t A =
-      strided ? 0u : static_cast<uint32_t>(min(static_cast<int64_t>(*reinterpret_cast<volatile unsigned*>(&p.ws->count)), p.T));
+  // planned path: the prefix of the per-chunk counts (the kernel entry waited for the planning
+  // pass), so that claim a maps to its chunk by a binary search in shared memory
+  const int nchunks = strided || !p.chunked ? 0 : static_cast<int>((p.T + kPlanTokensPerCta - 1) / kPlanTokensPerCta);
+  uint32_t A = strided || p.chunked ? 0u
+                                    : static_cast<uint32_t>(min(static_cast<int64_t>(*reinterpret_cast<volatile unsigned*>(&p.ws->count)), p.T));
+  for (int c0 = 0; c0 < nchunks; c0 += 32) {
+    const int c = c0 + lane;
+    const uint32_t n = c < nchunks ? static_cast<uint32_t>(list[p.T + c]) : 0u;
+    uint32_t incl = n;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    if (c < nchunks) S.chunk_prefix[c] = A + incl - n;
+    A += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  if (lane == 0 && nchunks > 0) S.chunk_prefix[nchunks] = A;
+  __syncwarp();
   int64_t next_t = blockIdx.x;  // token striding: this CTA's next candidate token
   uint32_t widx = 0;
   for (;;) {
@@ -153,7 +218,18 @@ __device__ void scheduler_warp(const Params& p, Smem& S, int lane) {
       if (lane == 0) a = atomicAdd(&p.ws->next, 1u);
       a = __shfl_sync(0xffffffffu, a, 0);
       end = a >= A;
-      if (!end && lane == 0) t = list[a];
+      if (!end && lane == 0) {
+        if (nchunks > 0) {
+          int lo = 0, hi = nchunks - 1;  // the last chunk whose prefix is <= a
+          while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (S.chunk_prefix[mid] <= a) lo = mid; else hi = mid - 1;
+          }
+          t = list[static_cast<int64_t>(lo) * kPlanTokensPerCta + (a - S.chunk_prefix[lo])];
+        } else {
+          t = list[a];  // the compact list of plan_kernel
+        }
+      }
     }
     if (!end) {
       if (lane == 0) {
@@ -336,12 +412,12 @@ __global__ void __launch_bounds__(kThreads, 1) compress_kernel(Params p) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
   Smem& S = *reinterpret_cast<Smem*>(smem_raw);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  // Token striding: launched as a programmatic dependent of the kernel before it on the stream
-  // (see direct_kernel). Planned path: a dependent of the planning kernel, whose results only the
-  // scheduler reads (after its own wait); what the other warps read was written before that
-  // kernel started.
+  // Launched as a programmatic dependent of the kernel before it on the stream: with token
+  // striding the previous call's kernel (or whatever precedes the call), on the planned path the
+  // planning pass, which itself waits for the kernel before it. Nothing global is touched before
+  // that kernel has completed; the next launch may start as soon as every CTA of this one runs.
   launch_dependents();
-  if (p.strided) grid_dependency_wait();
+  grid_dependency_wait();
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&S.full[s], 1);
@@ -715,11 +791,29 @@ cudaError_t launch(const Params& p, const LaunchCfg& cfg, cudaStream_t stream) {
     if (cfg.ev_end != nullptr) e = cudaEventRecord(cfg.ev_end, stream);
     return e;
   }
-  e = cudaMemsetAsync(p.ws, 0, 2 * sizeof(unsigned int), stream);  // count, next
-  if (e != cudaSuccess) return e;
+  // the planning pass: per-chunk lists (no zeroing pass, a programmatic dependent of the kernel
+  // before it) up to kMaxPlanChunks chunks, else the compact list after zeroing the counters
   const int plan_grid = static_cast<int>((p.T + kPlanTokensPerCta - 1) / kPlanTokensPerCta);
-  plan_kernel<<<plan_grid, kPlanThreads, 0, stream>>>(p);
-  e = cudaGetLastError();
+  Params q = p;
+  q.chunked = plan_grid <= kMaxPlanChunks;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  if (q.chunked) {
+    cudaLaunchConfig_t pc = {};
+    pc.gridDim = dim3(static_cast<unsigned>(plan_grid));
+    pc.blockDim = dim3(kPlanThreads);
+    pc.stream = stream;
+    pc.attrs = attr;
+    pc.numAttrs = cfg.pdl ? 1 : 0;
+    e = cudaLaunchKernelEx(&pc, plan_chunks_kernel, q);
+  } else {
+    e = cudaMemsetAsync(p.ws, 0, 2 * sizeof(unsigned int), stream);  // count, next
+    if (e == cudaSuccess) {
+      plan_kernel<<<plan_grid, kPlanThreads, 0, stream>>>(q);
+      e = cudaGetLastError();
+    }
+  }
   if (e != cudaSuccess) return e;
   if (cfg.ev_begin != nullptr && (e = cudaEventRecord(cfg.ev_begin, stream)) != cudaSuccess) return e;
   cudaLaunchConfig_t lc = {};
@@ -727,12 +821,9 @@ cudaError_t launch(const Params& p, const LaunchCfg& cfg, cudaStream_t stream) {
   lc.blockDim = dim3(kThreads);
   lc.dynamicSmemBytes = sizeof(Smem);
   lc.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
   lc.attrs = attr;
   lc.numAttrs = (cfg.pdl && cfg.ev_begin == nullptr) ? 1 : 0;
-  e = any_block ? cudaLaunchKernelEx(&lc, compress_kernel<true>, p) : cudaLaunchKernelEx(&lc, compress_kernel<false>, p);
+  e = any_block ? cudaLaunchKernelEx(&lc, compress_kernel<true>, q) : cudaLaunchKernelEx(&lc, compress_kernel<false>, q);
   if (e != cudaSuccess) return e;
   if (cfg.ev_end != nullptr) e = cudaEventRecord(cfg.ev_end, stream);
   return e;

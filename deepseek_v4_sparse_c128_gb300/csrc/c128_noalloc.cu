@@ -11,7 +11,9 @@
 namespace {
 
 constexpr int64_t kMaxTokens = C128_NOALLOC_MAX_TOKENS;
-constexpr size_t kScratchBytes = sizeof(c128::WsHeader) + static_cast<size_t>(kMaxTokens) * sizeof(int32_t);
+// header, then the token list and the per-chunk counts of the C128 planning pass
+constexpr size_t kScratchBytes =
+    sizeof(c128::WsHeader) + static_cast<size_t>(c128::plan_list_entries(kMaxTokens)) * sizeof(int32_t);
 
 // Lives in every GPU that loads the library. In host code this name is only a stand-in for the
 // symbol: the device address comes from cudaGetSymbolAddress.
@@ -69,6 +71,7 @@ extern "C" int c128_compress_norm_rope_store_noalloc(
   cfg.sm_count = d->sm_count;
   cfg.grid = static_cast<int>(p.T < d->sm_count ? p.T : d->sm_count);
   cfg.pdl = true;
-  // launch() zeroes the two counters the kernels start from before it enqueues them
+  // launch() resets what the kernels start from (the claim counter, and the counters or the
+  // per-chunk counts of the planning pass) before or while it runs them
   return c128::launch(p, cfg, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? C128_OK : C128_ERR_CUDA;
 }

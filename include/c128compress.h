@@ -203,9 +203,10 @@ int c128_compress_norm_rope_store_debug(const c128_tensor_t* token_to_req_indice
  * synchronisation) on the decode path, code running inside a memory-pool or allocator callback,
  * or a host that enforces a fixed device-memory budget. This entry point allocates nothing.
  *
- * Its scratch (a 256-byte header and the token list) is one static device array of
- * C128_NOALLOC_MAX_TOKENS tokens (256 KiB + 256 B) in the library image; every GPU that loads the
- * library holds it until the process exits. The first call on each device looks up that array's
+ * Its scratch (a 256-byte header, the token list and the planning pass's per-chunk counts) is one
+ * static device array for C128_NOALLOC_MAX_TOKENS tokens (256 KiB + 384 B) in the library image;
+ * every GPU that loads the library holds it until the process exits. The first call on each
+ * device looks up that array's
  * device address (cudaGetSymbolAddress, with that device current) and caches it; make that first
  * call before any stream capture. Arguments, layout and results are exactly those of
  * compress_norm_rope_store; T > C128_NOALLOC_MAX_TOKENS returns C128_ERR_TOO_MANY_TOKENS without

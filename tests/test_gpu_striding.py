@@ -81,3 +81,26 @@ def test_bad_indices_then_a_clean_call():
     kc, comp, err = run_gpu(q)
     assert err == 0
     assert check_against_oracle(q, kc, comp)["stored"] == 3
+
+
+def test_more_tokens_than_the_per_chunk_plan_covers():
+    """Above 2048 x 2048 tokens the planning pass falls back to one compact list behind a zeroing
+    pass: the mixed workload padded with inactive tokens to 4,194,305 tokens."""
+    import dataclasses
+    p = inputs.make_problem("mixed")
+    T = 2048 * 2048 + 1
+    pad = T - p.num_tokens
+    q = dataclasses.replace(
+        p, token_to_req=np.concatenate([p.token_to_req, np.zeros(pad, np.int32)]),
+        positions=np.concatenate([p.positions, np.full(pad, 127, np.int64)]),
+        slot_mapping=np.concatenate([p.slot_mapping, np.full(pad, -1, np.int64)]),
+        kv_slot_mapping=np.concatenate([p.kv_slot_mapping, np.zeros(pad, np.int64)]))
+    kc, comp, err = run_gpu(q, comp=False)
+    assert err == 0
+    ref = q.k_cache.copy()
+    oracle.forward(q, k_cache=ref, threads=16)
+    from gpu_util import slots_agree
+    rows = np.nonzero((q.slot_mapping >= 0) & ((q.positions + 1) % 128 == 0) & (q.kv_slot_mapping >= 0))[0]
+    assert rows.size > 10
+    differ, _, _ = slots_agree(q, kc, ref, rows)
+    assert differ <= 2  # rounding ties only
