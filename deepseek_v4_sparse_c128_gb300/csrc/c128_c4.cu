@@ -110,6 +110,7 @@ struct SmallSmem {
   uint64_t qfull[2];           // batch resolved (one arrival per scheduler lane)
   uint64_t qempty[2];          // batch taken (one arrival per copier lane)
   typename G::GroupSmem grp[G::kGroups];
+  uint32_t chunk_prefix[kMaxPlanChunks + 1];  // planned path: active windows before each chunk
   int abort_flag;
 };
 static_assert(sizeof(SmallSmem<512>) <= 227 * 1024 && sizeof(SmallSmem<128>) <= 227 * 1024, "shared memory");
@@ -174,11 +175,9 @@ __device__ void small_scheduler(const Params& p, SmallSmem<HEAD>& S, int lane, b
   // list mode: windows from plan_kernel's list; token striding (few tokens, no planning pass):
   // this CTA tests tokens c, c + grid, ..., 32 candidates per step
   const bool strided = p.strided != 0;
-  if (!strided) grid_dependency_wait();  // the list and the counters come from plan_kernel
-  const int32_t* list = reinterpret_cast<const int32_t*>(p.ws + 1);
   const volatile int* abort_flag = &S.abort_flag;
-  const uint32_t A =
-      strided ? 0u : static_cast<uint32_t>(min(static_cast<int64_t>(*reinterpret_cast<volatile unsigned*>(&p.ws->count)), p.T));
+  // planned path (the kernel entry waited for the planning pass): the list's windows
+  const uint32_t A = strided ? 0u : plan_prefix_warp(p, S.chunk_prefix, lane);
   const int n = (1 + p.overlap) * p.ratio;  // <= 8
   // claim size: 32 windows when there is plenty of work, else about one claim per CTA, so that a
   // small batch spreads over the SMs instead of a few CTAs taking 32 windows each
@@ -218,7 +217,7 @@ __device__ void small_scheduler(const Params& p, SmallSmem<HEAD>& S, int lane, b
       }
     } else {
       live = a < A && static_cast<uint32_t>(lane) < batch;
-      if (live) t = list[a];
+      if (live) t = plan_token(p, S.chunk_prefix, a);
     }
     int req = 0, nvalid = 0, ngroups = 0;
     int blk0 = 0, row0 = 0, half0 = 0, blk1 = 0, row1 = 0, half1 = 0;
@@ -656,12 +655,12 @@ __global__ void __launch_bounds__(SmallGeo<HEAD>::kThreads, 1)
   extern __shared__ __align__(128) unsigned char smem_raw[];
   SmallSmem<HEAD>& S = *reinterpret_cast<SmallSmem<HEAD>*>(smem_raw);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  // Token striding: a programmatic dependent of the kernel before it on the stream, so nothing
-  // global is touched before that kernel has completed; the next call may launch as soon as every
-  // CTA of this one runs. Planned path: a dependent of the planning kernel, whose results only the
-  // scheduler reads (after its own wait).
+  // A programmatic dependent of the kernel before it on the stream (with token striding the
+  // previous call's kernel or whatever precedes the call, on the planned path the planning pass,
+  // which itself waits for the kernel before it): nothing global is touched before that kernel has
+  // completed. The next launch may start as soon as every CTA of this one runs.
   launch_dependents();
-  if (p.strided) grid_dependency_wait();
+  grid_dependency_wait();
   if (tid == 0) {
     for (int s = 0; s < G::kStages; ++s) {
       mbar_init(&S.full[s], 1);

@@ -134,6 +134,44 @@ __device__ __forceinline__ bool consumer_bar_or(bool pred) {
 __device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" :::); }
 
+// ------------------------------------------------------------------ the planning pass's list
+// Read by one warp after the kernel waited for the planning pass: the number of active windows,
+// and with per-chunk lists the exclusive prefix of the chunk counts in prefix[0 .. nchunks]
+// (shared memory, kMaxPlanChunks + 1 words). Only this warp may use `prefix` afterwards.
+__device__ __noinline__ uint32_t plan_prefix_warp(const Params& p, uint32_t* prefix, int lane) {
+  const int32_t* list = reinterpret_cast<const int32_t*>(p.ws + 1);
+  if (!p.chunked)
+    return static_cast<uint32_t>(min(static_cast<int64_t>(*reinterpret_cast<const volatile unsigned*>(&p.ws->count)), p.T));
+  const int nchunks = static_cast<int>((p.T + kPlanTokensPerCta - 1) / kPlanTokensPerCta);
+  uint32_t A = 0;
+  for (int c0 = 0; c0 < nchunks; c0 += 32) {
+    const int c = c0 + lane;
+    const uint32_t n = c < nchunks ? static_cast<uint32_t>(list[p.T + c]) : 0u;
+    uint32_t incl = n;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    if (c < nchunks) prefix[c] = A + incl - n;
+    A += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  if (lane == 0) prefix[nchunks] = A;
+  __syncwarp();
+  return A;
+}
+// The token of claim a (a below the number of active windows).
+__device__ __forceinline__ int64_t plan_token(const Params& p, const uint32_t* prefix, uint32_t a) {
+  const int32_t* list = reinterpret_cast<const int32_t*>(p.ws + 1);
+  if (!p.chunked) return list[a];
+  int lo = 0, hi = static_cast<int>((p.T + kPlanTokensPerCta - 1) / kPlanTokensPerCta) - 1;
+  while (lo < hi) {  // the last chunk whose prefix is <= a
+    const int mid = (lo + hi + 1) >> 1;
+    if (prefix[mid] <= a) lo = mid; else hi = mid - 1;
+  }
+  return list[static_cast<int64_t>(lo) * kPlanTokensPerCta + (a - prefix[lo])];
+}
+
 // Consumer-only scratch of the fused epilogue (one window at a time).
 struct EpiSmem {
   unsigned long long red_lo[kConsumerWarps];

@@ -191,15 +191,23 @@ __global__ void __launch_bounds__(256, 3) gather_kernel(Params p) {
   const int tid = threadIdx.x;
   const int cg = tid % G::kColGroups, rg = tid / G::kColGroups;
   const int col = 4 * cg;
-  grid_dependency_wait();  // the list and its count come from plan_kernel
-  const int32_t* list = reinterpret_cast<const int32_t*>(p.ws + 1);
-  const int64_t A = min(static_cast<int64_t>(*reinterpret_cast<volatile unsigned*>(&p.ws->count)), p.T);
+  // a programmatic dependent of the planning pass (which waits for the kernel before it): nothing
+  // global is touched before it has completed
+  grid_dependency_wait();
+  __shared__ uint32_t chunk_prefix[kMaxPlanChunks + 1];
+  __shared__ uint32_t active;
+  if (tid < 32) {
+    const uint32_t a = plan_prefix_warp(p, chunk_prefix, tid);
+    if (tid == 0) active = a;
+  }
+  __syncthreads();
+  const int64_t A = active;
   const int nrows = (1 + p.overlap) * p.ratio;
   constexpr int kTokBytes = FMT == C128_FORMAT_SPARSE_FP8 ? kTokenStride : (FMT == C128_FORMAT_INDEXER_FP8 ? 128 : 64);
   constexpr int kScaleBytes = FMT == C128_FORMAT_SPARSE_FP8 ? kScaleDim : 4;
   for (int64_t a = blockIdx.x; a < A; a += gridDim.x) {
     __syncthreads();  // the previous window's epilogue is done with the shared scratch
-    const int64_t t = list[a];
+    const int64_t t = plan_token(p, chunk_prefix, static_cast<uint32_t>(a));
     const int req = __ldg(p.ttr + t);
     const int64_t pos = __ldg(p.pos + t), kvs = __ldg(p.kvslot + t);
     uint32_t err = 0;

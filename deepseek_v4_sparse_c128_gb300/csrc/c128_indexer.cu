@@ -80,6 +80,7 @@ struct IxSmem {
   } meta[2];
   uint64_t pfull[2];   // a window's partials written (one arrival per consumer warp)
   uint64_t pempty[2];  // the epilogue warp is done with them (one arrival)
+  uint32_t chunk_prefix[kMaxPlanChunks + 1];  // planned path: active windows before each chunk
   int abort_flag;
 };
 static_assert(sizeof(IxSmem) <= 227 * 1024, "shared memory");
@@ -109,11 +110,9 @@ __device__ void ix_scheduler(const Params& p, IxSmem& S, int lane) {
   // this CTA tests tokens c, c + grid, ..., 32 candidates per step. The mode is a template
   // parameter: with a run-time branch on it here, list-mode calls ran about 8 % slower.
   constexpr bool strided = STRIDED;
-  if (!strided) grid_dependency_wait();  // the list and the counters come from plan_kernel
-  const int32_t* list = reinterpret_cast<const int32_t*>(p.ws + 1);
   const volatile int* abort_flag = &S.abort_flag;
-  const uint32_t A =
-      strided ? 0u : static_cast<uint32_t>(min(static_cast<int64_t>(*reinterpret_cast<volatile unsigned*>(&p.ws->count)), p.T));
+  // planned path (the kernel entry waited for the planning pass): the list's windows
+  const uint32_t A = strided ? 0u : plan_prefix_warp(p, S.chunk_prefix, lane);
   int64_t next_t = blockIdx.x;
   const int n = (1 + p.overlap) * p.ratio;  // 16..256 rows, a multiple of 8
   uint32_t widx = 0;
@@ -148,7 +147,7 @@ __device__ void ix_scheduler(const Params& p, IxSmem& S, int lane) {
       a = __shfl_sync(0xffffffffu, a, 0);
       first_claim = false;
       end = a >= A;
-      if (!end && lane == 0) t = list[a];
+      if (!end && lane == 0) t = plan_token(p, S.chunk_prefix, a);
     }
     int req = 0;
     uint32_t err = 0;
@@ -437,12 +436,12 @@ __global__ void __launch_bounds__(kIxThreads, 1)
   extern __shared__ __align__(128) unsigned char smem_raw[];
   IxSmem& S = *reinterpret_cast<IxSmem*>(smem_raw);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  // Token striding: a programmatic dependent of the kernel before it on the stream, so nothing
-  // global is touched before that kernel has completed; the next call may launch as soon as every
-  // CTA of this one runs. Planned path: a dependent of the planning kernel, whose results only the
-  // scheduler reads (after its own wait).
+  // A programmatic dependent of the kernel before it on the stream (with token striding the
+  // previous call's kernel or whatever precedes the call, on the planned path the planning pass,
+  // which itself waits for the kernel before it): nothing global is touched before that kernel has
+  // completed. The next launch may start as soon as every CTA of this one runs.
   launch_dependents();
-  if (p.strided) grid_dependency_wait();
+  grid_dependency_wait();
   if (tid == 0) {
     for (int s = 0; s < kIxStages; ++s) {
       mbar_init(&S.full[s], 1);

@@ -36,21 +36,22 @@ constexpr int kPlanTokensPerThread = 8;
 constexpr int kPlanTokensPerCta = kPlanThreads * kPlanTokensPerThread;
 // Up to this many tokens per SM the C128 kernel runs without the planning pass (token striding).
 constexpr int kStridedTokensPerSm = 8;
-// The C128 planning pass writes, per chunk c of kPlanTokensPerCta tokens, its active tokens in
-// token order at list[c * kPlanTokensPerCta ...] and their number at list[T + c]: nothing
-// accumulates across CTAs or calls, so the pass needs no zeroed counters. The compress kernel's
-// scheduler keeps the prefix of the counts in shared memory, which bounds the chunks.
-constexpr int kMaxPlanChunks = 2048;  // token_num <= 2048 x 2048 = 4 Mi
+// The planning pass writes, per chunk c of kPlanTokensPerCta tokens, its active tokens in token
+// order at list[c * kPlanTokensPerCta ...] and their number at list[T + c]: nothing accumulates
+// across CTAs or calls, so the pass needs no zeroed counters. The kernels that take windows from
+// the list keep the prefix of the counts in shared memory, which bounds the chunks; above that a
+// compact list behind a zeroing pass serves.
+constexpr int kMaxPlanChunks = 512;  // token_num <= 512 x 2048 = 1 Mi
 // List entries (int32) the workspace needs for a call of `T` tokens: the list and the counts.
 constexpr int64_t plan_list_entries(int64_t T) { return T + (T + kPlanTokensPerCta - 1) / kPlanTokensPerCta; }
 constexpr unsigned long long kWaitTimeoutNs = 1000ull * 1000ull * 1000ull;  // 1 s per wait
 
 // Workspace layout: a 256-byte header then the list of active token indices.
 struct WsHeader {
-  unsigned int count;   // active windows found by the planning kernel (zeroed per call; not used
-                        // by the C128 path, whose planning pass writes per-chunk counts)
-  unsigned int next;    // next window to claim (zeroed per call: by a memset, or by the C128
-                        // planning pass)
+  unsigned int count;   // active windows of the compact list (zeroed per call; calls whose
+                        // planning pass writes per-chunk counts do not use it)
+  unsigned int next;    // next window to claim (zeroed per call: by a memset, or by the
+                        // per-chunk planning pass)
   unsigned int err;     // sticky C128_DEV_* bits
   unsigned int pad[61];
 };
@@ -82,7 +83,7 @@ struct Params {
   int32_t fmt;                // cache format (C128_FORMAT_*)
   int64_t sblk;               // state-cache block size (rows per block)
   int32_t strided;            // C128 kernel only: no planning pass, CTA c takes tokens c, c + grid, ...
-  int32_t chunked;            // C128 kernel, planned path: the list is per chunk (plan_chunks_kernel)
+  int32_t chunked;            // planned path: the list is per chunk (plan_chunks_kernel), else compact
   int32_t stall_first_window; // test only: one stage is armed but never filled (CTA 0's first in
                               // the compress and indexer kernels, the first listed window's in the
                               // small-window kernel)

@@ -154,27 +154,9 @@ struct Smem {
 template <bool ANY>
 __device__ void scheduler_warp(const Params& p, Smem& S, int lane) {
   const bool strided = p.strided != 0;
-  const int32_t* list = reinterpret_cast<const int32_t*>(p.ws + 1);
   const volatile int* abort_flag = &S.abort_flag;
-  // planned path: the prefix of the per-chunk counts (the kernel entry waited for the planning
-  // pass), so that claim a maps to its chunk by a binary search in shared memory
-  const int nchunks = strided || !p.chunked ? 0 : static_cast<int>((p.T + kPlanTokensPerCta - 1) / kPlanTokensPerCta);
-  uint32_t A = strided || p.chunked ? 0u
-                                    : static_cast<uint32_t>(min(static_cast<int64_t>(*reinterpret_cast<volatile unsigned*>(&p.ws->count)), p.T));
-  for (int c0 = 0; c0 < nchunks; c0 += 32) {
-    const int c = c0 + lane;
-    const uint32_t n = c < nchunks ? static_cast<uint32_t>(list[p.T + c]) : 0u;
-    uint32_t incl = n;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += v;
-    }
-    if (c < nchunks) S.chunk_prefix[c] = A + incl - n;
-    A += __shfl_sync(0xffffffffu, incl, 31);
-  }
-  if (lane == 0 && nchunks > 0) S.chunk_prefix[nchunks] = A;
-  __syncwarp();
+  // planned path (the kernel entry waited for the planning pass): the list's windows
+  const uint32_t A = strided ? 0u : plan_prefix_warp(p, S.chunk_prefix, lane);
   int64_t next_t = blockIdx.x;  // token striding: this CTA's next candidate token
   uint32_t widx = 0;
   for (;;) {
@@ -218,18 +200,7 @@ __device__ void scheduler_warp(const Params& p, Smem& S, int lane) {
       if (lane == 0) a = atomicAdd(&p.ws->next, 1u);
       a = __shfl_sync(0xffffffffu, a, 0);
       end = a >= A;
-      if (!end && lane == 0) {
-        if (nchunks > 0) {
-          int lo = 0, hi = nchunks - 1;  // the last chunk whose prefix is <= a
-          while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (S.chunk_prefix[mid] <= a) lo = mid; else hi = mid - 1;
-          }
-          t = list[static_cast<int64_t>(lo) * kPlanTokensPerCta + (a - S.chunk_prefix[lo])];
-        } else {
-          t = list[a];  // the compact list of plan_kernel
-        }
-      }
+      if (!end && lane == 0) t = plan_token(p, S.chunk_prefix, a);
     }
     if (!end) {
       if (lane == 0) {
@@ -730,6 +701,37 @@ cudaError_t prepare_device(int /*device*/) {
   return e;
 }
 
+namespace {
+// Enqueue the planning pass and return, in *q, the parameters of the kernel that takes windows from
+// its list: per-chunk lists (no zeroing pass) up to kMaxPlanChunks chunks, else the compact list
+// behind a zeroing of its counters. With `early`, the pass is a programmatic dependent of the
+// kernel before it (it launches while that kernel finishes and waits for it before any global
+// access). Not behind the head-512 small-window kernel: there every call took about 20 us longer
+// than its kernel (the 832-thread CTAs and the early pass did not overlap; measured, not
+// explained), against 1 us without the early launch.
+cudaError_t launch_plan(const Params& p, const LaunchCfg& cfg, cudaStream_t stream, Params* q, bool early) {
+  const int plan_grid = static_cast<int>((p.T + kPlanTokensPerCta - 1) / kPlanTokensPerCta);
+  *q = p;
+  q->chunked = plan_grid <= kMaxPlanChunks;
+  if (q->chunked) {
+    cudaLaunchConfig_t pc = {};
+    pc.gridDim = dim3(static_cast<unsigned>(plan_grid));
+    pc.blockDim = dim3(kPlanThreads);
+    pc.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    pc.attrs = attr;
+    pc.numAttrs = cfg.pdl && early ? 1 : 0;
+    return cudaLaunchKernelEx(&pc, plan_chunks_kernel, *q);
+  }
+  cudaError_t e = cudaMemsetAsync(p.ws, 0, 2 * sizeof(unsigned int), stream);  // count, next
+  if (e != cudaSuccess) return e;
+  plan_kernel<<<plan_grid, kPlanThreads, 0, stream>>>(*q);
+  return cudaGetLastError();
+}
+}  // namespace
+
 cudaError_t launch(const Params& p, const LaunchCfg& cfg, cudaStream_t stream) {
   if (!is_c128(p)) {
     cudaError_t e;
@@ -746,17 +748,14 @@ cudaError_t launch(const Params& p, const LaunchCfg& cfg, cudaStream_t stream) {
         return e;
       }
     }
-    e = cudaMemsetAsync(p.ws, 0, 2 * sizeof(unsigned int), stream);  // count, next
-    if (e != cudaSuccess) return e;
-    const int plan_grid = static_cast<int>((p.T + kPlanTokensPerCta - 1) / kPlanTokensPerCta);
-    plan_kernel<<<plan_grid, kPlanThreads, 0, stream>>>(p);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    Params q;
+    if ((e = launch_plan(p, cfg, stream, &q, !(small_window_path(p) && p.head == kHead))) != cudaSuccess) return e;
     if (cfg.ev_begin != nullptr && (e = cudaEventRecord(cfg.ev_begin, stream)) != cudaSuccess) return e;
-    if (small_window_path(p)) {
-      e = launch_small(p, cfg, stream);
+    if (small_window_path(q)) {
+      e = launch_small(q, cfg, stream);
     } else {
-      e = launch_indexer_windows(p, cfg, stream);
-      if (e == cudaErrorNotSupported) e = launch_gather(p, cfg, stream);
+      e = launch_indexer_windows(q, cfg, stream);
+      if (e == cudaErrorNotSupported) e = launch_gather(q, cfg, stream);
     }
     if (e != cudaSuccess) return e;
     if (cfg.ev_end != nullptr) e = cudaEventRecord(cfg.ev_end, stream);
@@ -791,29 +790,8 @@ cudaError_t launch(const Params& p, const LaunchCfg& cfg, cudaStream_t stream) {
     if (cfg.ev_end != nullptr) e = cudaEventRecord(cfg.ev_end, stream);
     return e;
   }
-  // the planning pass: per-chunk lists (no zeroing pass, a programmatic dependent of the kernel
-  // before it) up to kMaxPlanChunks chunks, else the compact list after zeroing the counters
-  const int plan_grid = static_cast<int>((p.T + kPlanTokensPerCta - 1) / kPlanTokensPerCta);
-  Params q = p;
-  q.chunked = plan_grid <= kMaxPlanChunks;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  if (q.chunked) {
-    cudaLaunchConfig_t pc = {};
-    pc.gridDim = dim3(static_cast<unsigned>(plan_grid));
-    pc.blockDim = dim3(kPlanThreads);
-    pc.stream = stream;
-    pc.attrs = attr;
-    pc.numAttrs = cfg.pdl ? 1 : 0;
-    e = cudaLaunchKernelEx(&pc, plan_chunks_kernel, q);
-  } else {
-    e = cudaMemsetAsync(p.ws, 0, 2 * sizeof(unsigned int), stream);  // count, next
-    if (e == cudaSuccess) {
-      plan_kernel<<<plan_grid, kPlanThreads, 0, stream>>>(q);
-      e = cudaGetLastError();
-    }
-  }
+  Params q;
+  e = launch_plan(p, cfg, stream, &q, true);
   if (e != cudaSuccess) return e;
   if (cfg.ev_begin != nullptr && (e = cudaEventRecord(cfg.ev_begin, stream)) != cudaSuccess) return e;
   cudaLaunchConfig_t lc = {};
@@ -821,6 +799,9 @@ cudaError_t launch(const Params& p, const LaunchCfg& cfg, cudaStream_t stream) {
   lc.blockDim = dim3(kThreads);
   lc.dynamicSmemBytes = sizeof(Smem);
   lc.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
   lc.attrs = attr;
   lc.numAttrs = (cfg.pdl && cfg.ev_begin == nullptr) ? 1 : 0;
   e = any_block ? cudaLaunchKernelEx(&lc, compress_kernel<true>, q) : cudaLaunchKernelEx(&lc, compress_kernel<false>, q);

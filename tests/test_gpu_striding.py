@@ -84,11 +84,11 @@ def test_bad_indices_then_a_clean_call():
 
 
 def test_more_tokens_than_the_per_chunk_plan_covers():
-    """Above 2048 x 2048 tokens the planning pass falls back to one compact list behind a zeroing
-    pass: the mixed workload padded with inactive tokens to 4,194,305 tokens."""
+    """Above 512 x 2048 tokens the planning pass falls back to one compact list behind a zeroing
+    pass: the mixed workload padded with inactive tokens to 1,048,577 tokens."""
     import dataclasses
     p = inputs.make_problem("mixed")
-    T = 2048 * 2048 + 1
+    T = 512 * 2048 + 1
     pad = T - p.num_tokens
     q = dataclasses.replace(
         p, token_to_req=np.concatenate([p.token_to_req, np.zeros(pad, np.int32)]),
