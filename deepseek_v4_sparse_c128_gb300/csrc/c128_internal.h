@@ -34,7 +34,8 @@ constexpr int kThreads = 64 + 32 * kConsumerWarps;  // scheduler warp, copy warp
 constexpr int kPlanThreads = 256;
 constexpr int kPlanTokensPerThread = 8;
 constexpr int kPlanTokensPerCta = kPlanThreads * kPlanTokensPerThread;
-// Up to this many tokens per SM the C128 kernel runs without the planning pass (token striding).
+// Up to this many tokens per SM the kernels run without the planning pass (C128: one CTA per
+// token; the other configurations: token striding).
 constexpr int kStridedTokensPerSm = 8;
 // The planning pass writes, per chunk c of kPlanTokensPerCta tokens, its active tokens in token
 // order at list[c * kPlanTokensPerCta ...] and their number at list[T + c]: nothing accumulates
@@ -82,11 +83,12 @@ struct Params {
   int32_t sw;                 // state width: kv columns of a row, as many score columns follow
   int32_t fmt;                // cache format (C128_FORMAT_*)
   int64_t sblk;               // state-cache block size (rows per block)
-  int32_t strided;            // C128 kernel only: no planning pass, CTA c takes tokens c, c + grid, ...
+  int32_t strided;            // small-window and indexer kernels: no planning pass, CTA c takes
+                              // tokens c, c + grid, ...
   int32_t chunked;            // planned path: the list is per chunk (plan_chunks_kernel), else compact
   int32_t stall_first_window; // test only: one stage is armed but never filled (CTA 0's first in
-                              // the compress and indexer kernels, the first listed window's in the
-                              // small-window kernel)
+                              // the compress, one-CTA-per-token and indexer kernels, the first
+                              // listed window's in the small-window kernel)
 };
 
 // True for the configurations the specialised C128 kernels serve: the C128 layout, with 8-row

@@ -1,8 +1,14 @@
 // sm_103a kernels of the DeepSeek-V4 C128 KV compressor.
 //
-//   plan_kernel      compacts the indices of active tokens (slot >= 0, position at a window end,
-//                    kv slot >= 0) into the workspace list; one pass over the per-token metadata.
-//   compress_kernel  persistent, one CTA per SM. Warp 0 claims windows from the list and resolves
+//   plan_chunks_kernel  the planning pass: per chunk of 2048 tokens, the indices of its active
+//                    tokens (slot >= 0, position at a window end, kv slot >= 0) in token order and
+//                    their number; plan_kernel compacts them into one list instead (above 1 Mi
+//                    tokens).
+//   direct_kernel    one token per cluster of S CTAs, no planning pass: S in {8, 4, 2, 1} while
+//                    token_num x S fits the SMs in one wave (the window split over the cluster,
+//                    merged over distributed shared memory), then up to 8 tokens per SM one CTA
+//                    per token with a 3-stage ring, two CTAs per SM.
+//   compress_kernel  above that: persistent, one CTA per SM. Warp 0 claims windows from the list and resolves
 //                    their 16 state blocks through the block table; warp 1 streams each block
 //                    (8 rows x 4 KiB = 32 KiB) into a 6-stage shared-memory ring with
 //                    cp.async.bulk (TMA bulk copies completing on mbarriers); warps 2..9 run an
@@ -153,62 +159,25 @@ struct Smem {
 
 template <bool ANY>
 __device__ void scheduler_warp(const Params& p, Smem& S, int lane) {
-  const bool strided = p.strided != 0;
   const volatile int* abort_flag = &S.abort_flag;
-  // planned path (the kernel entry waited for the planning pass): the list's windows
-  const uint32_t A = strided ? 0u : plan_prefix_warp(p, S.chunk_prefix, lane);
-  int64_t next_t = blockIdx.x;  // token striding: this CTA's next candidate token
+  // the planning pass's list (the kernel entry waited for that pass)
+  const uint32_t A = plan_prefix_warp(p, S.chunk_prefix, lane);
   uint32_t widx = 0;
   for (;;) {
     if (*abort_flag) return;
-    bool end;
     long long t = 0, pos = 0, kvs = 0;
     int req = 0;
     uint32_t err = 0;
-    if (strided) {
-      // the next active token among next_t, next_t + grid, ...: 32 candidates per step; the
-      // candidates' request, position and kv slot come with the test, from the lane that found it
-      long long found = -1;
-      while (found < 0 && next_t < p.T) {
-        const int64_t c = next_t + static_cast<int64_t>(lane) * gridDim.x;
-        bool act = false;
-        long long ps = 0, kv = 0;
-        int rq = 0;
-        if (c < p.T) {
-          const int64_t s = __ldg(p.slot + c);
-          ps = __ldg(p.pos + c);
-          kv = __ldg(p.kvslot + c);
-          rq = __ldg(p.ttr + c);
-          act = (s >= 0) & (ps >= 0) & (((ps + 1) & (kRatio - 1)) == 0) & (kv >= 0);
-        }
-        const uint32_t m = __ballot_sync(0xffffffffu, act);
-        if (m) {
-          const int src = __ffs(m) - 1;
-          found = next_t + static_cast<int64_t>(src) * gridDim.x;
-          next_t = found + gridDim.x;
-          pos = __shfl_sync(0xffffffffu, ps, src);
-          kvs = __shfl_sync(0xffffffffu, kv, src);
-          req = __shfl_sync(0xffffffffu, rq, src);
-        } else {
-          next_t += 32ll * gridDim.x;
-        }
-      }
-      end = found < 0;
-      if (!end && lane == 0) t = found;
-    } else {
-      uint32_t a = 0;
-      if (lane == 0) a = atomicAdd(&p.ws->next, 1u);
-      a = __shfl_sync(0xffffffffu, a, 0);
-      end = a >= A;
-      if (!end && lane == 0) t = plan_token(p, S.chunk_prefix, a);
-    }
+    uint32_t a = 0;
+    if (lane == 0) a = atomicAdd(&p.ws->next, 1u);
+    a = __shfl_sync(0xffffffffu, a, 0);
+    const bool end = a >= A;
+    if (!end && lane == 0) t = plan_token(p, S.chunk_prefix, a);
     if (!end) {
       if (lane == 0) {
-        if (!strided) {
-          req = __ldg(p.ttr + t);
-          pos = __ldg(p.pos + t);
-          kvs = __ldg(p.kvslot + t);
-        }
+        req = __ldg(p.ttr + t);
+        pos = __ldg(p.pos + t);
+        kvs = __ldg(p.kvslot + t);
         if (req < 0 || req >= p.bt_rows) err |= C128_DEV_BAD_REQ;
         if ((ANY ? pos / p.sblk : pos / kStateBlock) >= p.bt_cols) err |= C128_DEV_BAD_BT_COL;
         if (pos - (kRatio - 1) >= p.cs_rows) err |= C128_DEV_BAD_COS_ROW;  // (p/128)*128 == p-127
@@ -383,10 +352,9 @@ __global__ void __launch_bounds__(kThreads, 1) compress_kernel(Params p) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
   Smem& S = *reinterpret_cast<Smem*>(smem_raw);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  // Launched as a programmatic dependent of the kernel before it on the stream: with token
-  // striding the previous call's kernel (or whatever precedes the call), on the planned path the
-  // planning pass, which itself waits for the kernel before it. Nothing global is touched before
-  // that kernel has completed; the next launch may start as soon as every CTA of this one runs.
+  // Launched as a programmatic dependent of the planning pass, which itself waits for the kernel
+  // before it: nothing global is touched before that pass has completed. The next launch may
+  // start as soon as every CTA of this one runs.
   launch_dependents();
   grid_dependency_wait();
   if (tid == 0) {
@@ -417,17 +385,23 @@ __global__ void __launch_bounds__(kThreads, 1) compress_kernel(Params p) {
 // them into partial softmax states, rank 0 merges the S partials from distributed shared memory
 // (in rank order) and runs the same epilogue. Every CTA of a cluster reads the same token and all
 // 16 block ids, so every early exit is uniform across the cluster.
-template <int S>
+// R: ring depth; 0 = as deep as the CTA's blocks allow up to kStages (one CTA per SM). A shallower
+// ring lets several CTAs share an SM, so that one CTA's start overlaps another's stream.
+template <int S, int R = 0>
 struct DirectCfg {
   static constexpr int kBlocks = kWindowBlocks / S;                 // stages per CTA
-  static constexpr int kRing = kBlocks < kStages ? kBlocks : kStages;
+  static constexpr int kDeep = kBlocks < kStages ? kBlocks : kStages;
+  static constexpr int kRing = R > 0 && R < kDeep ? R : kDeep;
 };
 
-template <int S>
+constexpr int kMidRing = 3;  // ring of the one-CTA-per-token kernel (more tokens than SMs)
+static_assert(2 * (kMidRing * kStageBytes + 12 * 1024) <= 227 * 1024, "two such CTAs per SM");
+
+template <int S, int R = 0>
 struct DirectSmem {
-  float stage[DirectCfg<S>::kRing][kStateBlock * kRow];
-  uint64_t full[DirectCfg<S>::kRing];
-  uint64_t empty[DirectCfg<S>::kRing];
+  float stage[DirectCfg<S, R>::kRing][kStateBlock * kRow];
+  uint64_t full[DirectCfg<S, R>::kRing];
+  uint64_t empty[DirectCfg<S, R>::kRing];
   float2 part_m[kHead / 2];   // partial softmax state of this CTA's rows, per column pair
   float2 part_l[kHead / 2];
   float2 part_a[kHead / 2];
@@ -461,11 +435,11 @@ __device__ __forceinline__ int ld_cluster_s32(uint32_t addr) {
   return v;
 }
 
-template <int S, bool ANY>
-__global__ void __launch_bounds__(kThreads, 1) direct_kernel(Params p) {
-  using Cfg = DirectCfg<S>;
+template <int S, bool ANY, int R = 0>
+__global__ void __launch_bounds__(kThreads, R > 0 ? 2 : 1) direct_kernel(Params p) {
+  using Cfg = DirectCfg<S, R>;
   extern __shared__ __align__(128) unsigned char smem_raw[];
-  DirectSmem<S>& D = *reinterpret_cast<DirectSmem<S>*>(smem_raw);
+  DirectSmem<S, R>& D = *reinterpret_cast<DirectSmem<S, R>*>(smem_raw);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t rank = S > 1 ? cluster_ctarank() : 0u;
   const int64_t t = static_cast<int64_t>(blockIdx.x) / S;
@@ -478,6 +452,8 @@ __global__ void __launch_bounds__(kThreads, 1) direct_kernel(Params p) {
   // latency overlaps it
   const int64_t slot = __ldg(p.slot + t), pos = __ldg(p.pos + t), kvs = __ldg(p.kvslot + t);
   const int req = __ldg(p.ttr + t);
+  // an inactive token's CTAs leave at once (uniformly: every CTA of a cluster reads the same token)
+  if (!((slot >= 0) & (pos >= 0) & ((pos & (kRatio - 1)) == kRatio - 1) & (kvs >= 0))) return;
   if (tid == 0) {
     for (int s = 0; s < Cfg::kRing; ++s) {
       mbar_init(&D.full[s], 1);
@@ -491,7 +467,6 @@ __global__ void __launch_bounds__(kThreads, 1) direct_kernel(Params p) {
   const volatile int* abort_flag = &D.abort_flag;
 
   // the token's window
-  if (!((slot >= 0) & (pos >= 0) & ((pos & (kRatio - 1)) == kRatio - 1) & (kvs >= 0))) return;
   uint32_t err = 0;
   if (req < 0 || req >= p.bt_rows) err |= C128_DEV_BAD_REQ;
   if ((ANY ? pos / p.sblk : pos / kStateBlock) >= p.bt_cols) err |= C128_DEV_BAD_BT_COL;
@@ -537,7 +512,10 @@ __global__ void __launch_bounds__(kThreads, 1) direct_kernel(Params p) {
             o += ((pos - (kRatio - 1) + static_cast<long long>(kStateBlock) * (static_cast<int>(rank) * Cfg::kBlocks + j)) %
                   p.sblk) * p.s1;
           const float* src = p.state + o;
-          if (p.s1 == kRow) {
+          if (p.stall_first_window && blockIdx.x == 0 && j == 0) {
+            // test of the bounded waits: this stage never fills, so the consumers give up after
+            // the time limit and the kernel reports C128_DEV_TIMEOUT instead of hanging
+          } else if (p.s1 == kRow) {
             bulk_copy_g2s(D.stage[s], src, kStageBytes, &D.full[s], policy);
           } else {
             for (int r = 0; r < kStateBlock; ++r)
@@ -642,7 +620,7 @@ int direct_split(int64_t T, int sm_count) {
   return 1;
 }
 
-template <int S, bool ANY>
+template <int S, bool ANY, int R = 0>
 cudaError_t launch_direct(const Params& p, const LaunchCfg& cfg, cudaStream_t stream) {
   if (cfg.ev_begin != nullptr) {
     const cudaError_t e = cudaEventRecord(cfg.ev_begin, stream);
@@ -651,7 +629,7 @@ cudaError_t launch_direct(const Params& p, const LaunchCfg& cfg, cudaStream_t st
   cudaLaunchConfig_t lc = {};
   lc.gridDim = dim3(static_cast<unsigned>(p.T * S));
   lc.blockDim = dim3(kThreads);
-  lc.dynamicSmemBytes = sizeof(DirectSmem<S>);
+  lc.dynamicSmemBytes = sizeof(DirectSmem<S, R>);
   lc.stream = stream;
   cudaLaunchAttribute attr[2];
   unsigned n = 0;
@@ -669,7 +647,7 @@ cudaError_t launch_direct(const Params& p, const LaunchCfg& cfg, cudaStream_t st
   }
   lc.attrs = attr;
   lc.numAttrs = n;
-  cudaError_t e = cudaLaunchKernelEx(&lc, direct_kernel<S, ANY>, p);
+  cudaError_t e = cudaLaunchKernelEx(&lc, direct_kernel<S, ANY, R>, p);
   if (e != cudaSuccess) return e;
   if (cfg.ev_end != nullptr) e = cudaEventRecord(cfg.ev_end, stream);
   return e;
@@ -686,6 +664,10 @@ cudaError_t set_direct_smem(cudaFuncAttribute a) {
   if (e == cudaSuccess) e = cudaFuncSetAttribute(direct_kernel<2, ANY>, a, static_cast<int>(sizeof(DirectSmem<2>)));
   if (e == cudaSuccess) e = cudaFuncSetAttribute(direct_kernel<4, ANY>, a, static_cast<int>(sizeof(DirectSmem<4>)));
   if (e == cudaSuccess) e = cudaFuncSetAttribute(direct_kernel<8, ANY>, a, static_cast<int>(sizeof(DirectSmem<8>)));
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(direct_kernel<1, ANY, kMidRing>, a, static_cast<int>(sizeof(DirectSmem<1, kMidRing>)));
+  if (e == cudaSuccess)  // all of the SM's shared memory, for two of these CTAs
+    e = cudaFuncSetAttribute(direct_kernel<1, ANY, kMidRing>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
   return e;
 }
 }  // namespace
@@ -770,26 +752,10 @@ cudaError_t launch(const Params& p, const LaunchCfg& cfg, cudaStream_t stream) {
     default: break;
   }
   cudaError_t e;
-  if (p.T <= static_cast<int64_t>(kStridedTokensPerSm) * cfg.sm_count) {
-    // few tokens per SM: no planning pass, no counters; CTA c takes tokens c, c + grid, ...
-    Params q = p;
-    q.strided = 1;
-    if (cfg.ev_begin != nullptr && (e = cudaEventRecord(cfg.ev_begin, stream)) != cudaSuccess) return e;
-    cudaLaunchConfig_t lc = {};
-    lc.gridDim = dim3(static_cast<unsigned>(cfg.grid));
-    lc.blockDim = dim3(kThreads);
-    lc.dynamicSmemBytes = sizeof(Smem);
-    lc.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    lc.attrs = attr;
-    lc.numAttrs = (cfg.pdl && cfg.ev_begin == nullptr) ? 1 : 0;
-    e = any_block ? cudaLaunchKernelEx(&lc, compress_kernel<true>, q) : cudaLaunchKernelEx(&lc, compress_kernel<false>, q);
-    if (e != cudaSuccess) return e;
-    if (cfg.ev_end != nullptr) e = cudaEventRecord(cfg.ev_end, stream);
-    return e;
-  }
+  // up to 8 tokens per SM: one CTA per token with a 3-stage ring, two CTAs per SM, so that the
+  // hardware deals the windows out and one CTA's start and epilogue overlap another's stream
+  if (p.T <= static_cast<int64_t>(kStridedTokensPerSm) * cfg.sm_count)
+    return any_block ? launch_direct<1, true, kMidRing>(p, cfg, stream) : launch_direct<1, false, kMidRing>(p, cfg, stream);
   Params q;
   e = launch_plan(p, cfg, stream, &q, true);
   if (e != cudaSuccess) return e;

@@ -150,14 +150,15 @@ int compress_norm_rope_store(const c128_tensor_t* token_to_req_indices,
 
 /*
  * Test of the failure handling, for tests only. Runs compress_norm_rope_store on the same
- * arguments (C128 layout), except that CTA 0 of the compress kernel arms the first stage of its
- * first window and never copies into it. Every wait in the kernels is bounded (1 s), so the
- * consumers of that stage give up, the CTA stops, and the kernel ends with C128_DEV_TIMEOUT in
- * the device error bits (read them with c128_device_errors) instead of hanging; the CUDA context
- * stays usable. Other CTAs store their windows as usual; CTA 0's windows are not stored. Takes
- * about two seconds of GPU time. Returns C128_ERR_ARG when the batch has no more tokens than the
- * GPU has SMs (such batches run the cluster-split kernel, which has no copy warp to stall), else
- * the codes of compress_norm_rope_store.
+ * arguments (C128 layout), except that CTA 0 arms the first stage of its first window and never
+ * copies into it (the one-CTA-per-token kernel up to 8 tokens per SM, the compress kernel above).
+ * Every wait in the kernels is bounded (1 s), so the consumers of that stage give up, the CTA
+ * stops, and the kernel ends with C128_DEV_TIMEOUT in the device error bits (read them with
+ * c128_device_errors) instead of hanging; the CUDA context stays usable. Other CTAs store their
+ * windows as usual; CTA 0's windows are not stored. Takes about two seconds of GPU time. Returns
+ * C128_ERR_ARG when the batch has no more tokens than the GPU has SMs (such batches run the
+ * cluster-split kernel, which is not set up for this test), else the codes of
+ * compress_norm_rope_store.
  */
 int c128_debug_stall_first_window(const c128_tensor_t* token_to_req_indices,
                                   const c128_tensor_t* positions,
