@@ -444,7 +444,61 @@ __device__ void small_copier(const Params& p, SmallSmem<HEAD>& S, int lane, cons
   }
 }
 
-// Softmax-weighted sum of 4 consecutive columns `col` over the window's present rows.
+// A window's present rows for 4 consecutive columns: score and kv quads, oldest row first.
+struct WindowCols {
+  float4 sc[kMaxSmallRows];
+  float4 kv[kMaxSmallRows];
+};
+
+template <int HEAD>
+__device__ __forceinline__ void stage_load(const float* st, int nvalid, int col, WindowCols& w) {
+  constexpr int R = 2 * HEAD;
+#pragma unroll
+  for (int i = 0; i < kMaxSmallRows; ++i) {
+    if (i < nvalid) {
+      w.sc[i] = *reinterpret_cast<const float4*>(st + i * R + HEAD + col);
+      w.kv[i] = *reinterpret_cast<const float4*>(st + i * R + col);
+    }
+  }
+}
+
+// Softmax-weighted sum over the window's present rows, column by column.
+__device__ __forceinline__ float4 window_comp(const WindowCols& w, int nvalid) {
+  float4 mx = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+#pragma unroll
+  for (int i = 0; i < kMaxSmallRows; ++i) {
+    if (i < nvalid) {
+      mx.x = fmaxf(mx.x, w.sc[i].x);
+      mx.y = fmaxf(mx.y, w.sc[i].y);
+      mx.z = fmaxf(mx.z, w.sc[i].z);
+      mx.w = fmaxf(mx.w, w.sc[i].w);
+    }
+  }
+  const float4 bias = make_float4(mx.x * kLog2e, mx.y * kLog2e, mx.z * kLog2e, mx.w * kLog2e);
+  float4 l = make_float4(0.f, 0.f, 0.f, 0.f), acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+  for (int i = 0; i < kMaxSmallRows; ++i) {
+    if (i < nvalid) {
+      const float4 kv = w.kv[i];
+      const float ex = ex2_approx(fmaf(w.sc[i].x, kLog2e, -bias.x));
+      const float ey = ex2_approx(fmaf(w.sc[i].y, kLog2e, -bias.y));
+      const float ez = ex2_approx(fmaf(w.sc[i].z, kLog2e, -bias.z));
+      const float ew = ex2_approx(fmaf(w.sc[i].w, kLog2e, -bias.w));
+      l.x += ex;
+      l.y += ey;
+      l.z += ez;
+      l.w += ew;
+      acc.x = fmaf(ex, kv.x, acc.x);
+      acc.y = fmaf(ey, kv.y, acc.y);
+      acc.z = fmaf(ez, kv.z, acc.z);
+      acc.w = fmaf(ew, kv.w, acc.w);
+    }
+  }
+  return make_float4(__fdiv_rn(acc.x, l.x), __fdiv_rn(acc.y, l.y), __fdiv_rn(acc.z, l.z), __fdiv_rn(acc.w, l.w));
+}
+
+// Softmax-weighted sum of 4 consecutive columns `col` over the window's present rows, read from
+// the stage as the arithmetic needs them.
 template <int HEAD>
 __device__ __forceinline__ float4 stage_comp(const float* st, int nvalid, int col) {
   constexpr int R = 2 * HEAD;
@@ -627,12 +681,12 @@ __device__ void small_indexer_warp(const Params& p, SmallSmem<128>& S, int w, in
       if (lane == 0) mbar_arrive(&S.empty[sl]);
       continue;
     }
-    const float4 c = stage_comp<128>(S.stage[sl], nvalid, col);
     const SmallDesc& d = S.desc[sl];
     uint8_t* tok = d.tok;
     uint8_t* scale = d.scale;
     float* comp_dst = d.comp_dst;
-    // pairs j = 2*lane, 2*lane + 1; pairs >= 32 (lanes 16..31) rotate, the others use cos 1, sin 0
+    // pairs j = 2*lane, 2*lane + 1; pairs >= 32 (lanes 16..31) rotate, the others use cos 1, sin 0.
+    // The cos/sin loads go out first and land while the window is folded.
     float2 cosv = make_float2(1.f, 1.f), sinv = make_float2(0.f, 0.f);
     if (lane >= 16) {
       const int j0 = 2 * lane - 32;
@@ -640,8 +694,13 @@ __device__ void small_indexer_warp(const Params& p, SmallSmem<128>& S, int w, in
       cosv = make_float2(__ldg(cs + j0), __ldg(cs + j0 + 1));
       sinv = make_float2(__ldg(cs + kRope / 2 + j0), __ldg(cs + kRope / 2 + j0 + 1));
     }
+    // the window's rows go to registers and the stage is released before the arithmetic, so the
+    // copier can refill it while this warp folds the window and runs the epilogue
+    WindowCols wc;
+    stage_load<128>(S.stage[sl], nvalid, col, wc);
     __syncwarp();
     if (lane == 0) mbar_arrive(&S.empty[sl]);
+    const float4 c = window_comp(wc, nvalid);
 
     indexer_warp_epilogue<FMT>(c, lane, wa, wb, p.eps, cosv, sinv, tok, scale, comp_dst, comp_s);
   }

@@ -143,17 +143,27 @@ __device__ __noinline__ uint32_t plan_prefix_warp(const Params& p, uint32_t* pre
   if (!p.chunked)
     return static_cast<uint32_t>(min(static_cast<int64_t>(*reinterpret_cast<const volatile unsigned*>(&p.ws->count)), p.T));
   const int nchunks = static_cast<int>((p.T + kPlanTokensPerCta - 1) / kPlanTokensPerCta);
+  // All counts are loaded before the first is used: one global round trip instead of one per
+  // 32 chunks (a round trip from a busy SM costs microseconds, and this sits in front of the
+  // kernel's first copy).
+  constexpr int kPerLane = kMaxPlanChunks / 32;
+  uint32_t n[kPerLane];
+#pragma unroll
+  for (int i = 0; i < kPerLane; ++i) {
+    const int c = 32 * i + lane;
+    n[i] = c < nchunks ? static_cast<uint32_t>(list[p.T + c]) : 0u;
+  }
   uint32_t A = 0;
-  for (int c0 = 0; c0 < nchunks; c0 += 32) {
-    const int c = c0 + lane;
-    const uint32_t n = c < nchunks ? static_cast<uint32_t>(list[p.T + c]) : 0u;
-    uint32_t incl = n;
+#pragma unroll
+  for (int i = 0; i < kPerLane; ++i) {
+    if (32 * i >= nchunks) break;
+    uint32_t incl = n[i];
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
       if (lane >= o) incl += v;
     }
-    if (c < nchunks) prefix[c] = A + incl - n;
+    if (32 * i + lane < nchunks) prefix[32 * i + lane] = A + incl - n[i];
     A += __shfl_sync(0xffffffffu, incl, 31);
   }
   if (lane == 0) prefix[nchunks] = A;
@@ -277,14 +287,21 @@ __device__ __forceinline__ void online_init(Online& o) {
   o.m0 = o.m1 = -INFINITY;
   o.l0 = o.l1 = o.a0 = o.a1 = 0.f;
 }
-// Fold the 8 rows of one staged state block into the state of columns c0, c0 + 1.
-__device__ __forceinline__ void online_stage(const float* st, int c0, Online& o) {
+// The 8 rows of one staged state block for columns c0, c0 + 1: kv and score pairs.
+struct BlockRows {
   float2 kv[kStateBlock], sc[kStateBlock];
+};
+__device__ __forceinline__ void stage_rows(const float* st, int c0, BlockRows& br) {
 #pragma unroll
   for (int r = 0; r < kStateBlock; ++r) {
-    kv[r] = *reinterpret_cast<const float2*>(st + r * kRow + c0);
-    sc[r] = *reinterpret_cast<const float2*>(st + r * kRow + kHead + c0);
+    br.kv[r] = *reinterpret_cast<const float2*>(st + r * kRow + c0);
+    br.sc[r] = *reinterpret_cast<const float2*>(st + r * kRow + kHead + c0);
   }
+}
+// Fold those rows into the state of columns c0, c0 + 1.
+__device__ __forceinline__ void online_fold(const BlockRows& br, Online& o) {
+  const float2* kv = br.kv;
+  const float2* sc = br.sc;
   float mx0 = sc[0].x, mx1 = sc[0].y;
 #pragma unroll
   for (int r = 1; r < kStateBlock; ++r) {

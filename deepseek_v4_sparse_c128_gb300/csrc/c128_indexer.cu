@@ -273,14 +273,21 @@ __device__ void ix_copier(const Params& p, IxSmem& S, const CUtensorMap* map) {
 }
 
 // ------------------------------------------------------------------------------ consumer warps
-// Fold the 8 rows of one staged chunk into the online state of columns c0, c0 + 1.
-__device__ __forceinline__ void ix_fold_chunk(const float* st, int c0, Online& o) {
+// The 8 rows of one staged chunk for columns c0, c0 + 1: kv and score pairs.
+struct ChunkRows {
   float2 kv[kIxChunk], sc[kIxChunk];
+};
+__device__ __forceinline__ void ix_load_chunk(const float* st, int c0, ChunkRows& cr) {
 #pragma unroll
   for (int r = 0; r < kIxChunk; ++r) {
-    kv[r] = *reinterpret_cast<const float2*>(st + r * kIxRowFloats + c0);
-    sc[r] = *reinterpret_cast<const float2*>(st + r * kIxRowFloats + kIxHead + c0);
+    cr.kv[r] = *reinterpret_cast<const float2*>(st + r * kIxRowFloats + c0);
+    cr.sc[r] = *reinterpret_cast<const float2*>(st + r * kIxRowFloats + kIxHead + c0);
   }
+}
+// Fold those rows into the online state of columns c0, c0 + 1.
+__device__ __forceinline__ void ix_fold_chunk(const ChunkRows& cr, Online& o) {
+  const float2* kv = cr.kv;
+  const float2* sc = cr.sc;
   float mx0 = sc[0].x, mx1 = sc[0].y;
 #pragma unroll
   for (int r = 1; r < kIxChunk; ++r) {
@@ -361,9 +368,14 @@ __device__ void ix_consumers(const Params& p, IxSmem& S, int ci) {
       bool ok = !failed && mbar_wait_suspend(&S.full[s], (it / kIxStages) & 1u, abort_flag);
       ok = __all_sync(0xffffffffu, ok);
       if (ok) {
-        if (cs0 + rg < nch) ix_fold_chunk(S.stage[s] + rg * kIxChunkFloats, c0, o);
+        // the rows go to registers and the stage is released before the arithmetic, so the copier
+        // can refill it while the warp folds the chunk
+        const bool mine = cs0 + rg < nch;
+        ChunkRows cr;
+        if (mine) ix_load_chunk(S.stage[s] + rg * kIxChunkFloats, c0, cr);
         __syncwarp();
         if (lane == 0) mbar_arrive(&S.empty[s]);
+        if (mine) ix_fold_chunk(cr, o);
       } else {
         failed = true;
       }

@@ -51,8 +51,8 @@ constexpr unsigned long long kWaitTimeoutNs = 1000ull * 1000ull * 1000ull;  // 1
 struct WsHeader {
   unsigned int count;   // active windows of the compact list (zeroed per call; calls whose
                         // planning pass writes per-chunk counts do not use it)
-  unsigned int next;    // next window to claim (zeroed per call: by a memset, or by the
-                        // per-chunk planning pass)
+  unsigned int next;    // the window kernels' shared claim counter (zeroed per call: by a
+                        // memset, or by the per-chunk planning pass)
   unsigned int err;     // sticky C128_DEV_* bits
   unsigned int pad[61];
 };

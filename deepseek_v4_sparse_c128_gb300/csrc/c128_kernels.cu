@@ -163,13 +163,15 @@ __device__ void scheduler_warp(const Params& p, Smem& S, int lane) {
   // the planning pass's list (the kernel entry waited for that pass)
   const uint32_t A = plan_prefix_warp(p, S.chunk_prefix, lane);
   uint32_t widx = 0;
-  for (;;) {
+  for (bool first_claim = true;; first_claim = false) {
     if (*abort_flag) return;
     long long t = 0, pos = 0, kvs = 0;
     int req = 0;
     uint32_t err = 0;
+    // the first claim is static (CTA b takes window b), which takes a global round trip off the
+    // way to the first copy; the rest come from the shared counter
     uint32_t a = 0;
-    if (lane == 0) a = atomicAdd(&p.ws->next, 1u);
+    if (lane == 0) a = first_claim ? blockIdx.x : gridDim.x + atomicAdd(&p.ws->next, 1u);
     a = __shfl_sync(0xffffffffu, a, 0);
     const bool end = a >= A;
     if (!end && lane == 0) t = plan_token(p, S.chunk_prefix, a);
@@ -327,9 +329,12 @@ __device__ void consumer_warps(const Params& p, Smem& S, int ci) {
       bool ok = !failed && mbar_wait(&S.full[s], (it / kStages) & 1u, abort_flag);
       ok = __all_sync(0xffffffffu, ok);
       if (ok) {
-        online_stage(S.stage[s], c0, o);
+        // the rows go to registers and the stage is released before the arithmetic
+        BlockRows br;
+        stage_rows(S.stage[s], c0, br);
         __syncwarp();
         if (lane == 0) mbar_arrive(&S.empty[s]);
+        online_fold(br, o);
       } else {
         failed = true;
       }
@@ -537,9 +542,12 @@ __global__ void __launch_bounds__(kThreads, R > 0 ? 2 : 1) direct_kernel(Params 
       bool ok = !failed && mbar_wait(&D.full[s], (j / Cfg::kRing) & 1u, abort_flag);
       ok = __all_sync(0xffffffffu, ok);
       if (ok) {
-        online_stage(D.stage[s], c0, o);
+        // the rows go to registers and the stage is released before the arithmetic
+        BlockRows br;
+        stage_rows(D.stage[s], c0, br);
         __syncwarp();
         if (lane == 0) mbar_arrive(&D.empty[s]);
+        online_fold(br, o);
       } else {
         failed = true;
       }
