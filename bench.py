@@ -401,7 +401,7 @@ def read_probe_rate(buf, stream, launches: int = 10) -> dict:
 
 def launches_per_call(T: int, sm_count: int) -> int:
     """Kernels one C128 call launches: the cluster-split kernel for T x S <= #SM (S >= 1), the
-    token-striding kernel up to 8 tokens per SM, else the planning kernel and the compress kernel."""
+    one-CTA-per-token kernel up to 8 tokens per SM, else the planning kernel and the compress kernel."""
     return 1 if T <= 8 * sm_count else 2
 
 

@@ -1,5 +1,5 @@
 """Out-of-bounds writes: k_cache and the fp32 export each sit inside a larger device buffer filled
-with random canary bytes, for every kernel path (cluster-split, token striding, planning pass +
+with random canary bytes, for every kernel path (cluster-split, one CTA per token, planning pass +
 window queue, the small-window ring, the ratio-128 indexer ring, the gather kernel). After the
 call, every canary byte must be unchanged and the bytes inside must match the oracle."""
 import numpy as np

@@ -5,7 +5,7 @@
   rows and nothing may overflow;
 - scores offset by +1e4 or -1e4 per state block: large magnitudes, where within a window the
   blocks with the lower offset get weights that underflow to 0.
-Each on every C128 call path (cluster split, token striding, planning pass); and -inf scores in
+Each on every C128 call path (cluster split, one CTA per token, planning pass); and -inf scores in
 the four other configurations."""
 import numpy as np
 import pytest

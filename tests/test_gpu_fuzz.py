@@ -4,7 +4,7 @@ compress_norm_rope_store_ex: cache format, compress ratio (1..256), overlap, sta
 (1..64), kv block size (odd ones included), request count and lengths, decode tails; each case
 takes whichever kernel its configuration selects (small-window ring with tiled or per-row copies,
 indexer ring, gather). compress_norm_rope_store: random batches of 1..5000 tokens over its three
-call paths (cluster split, token striding, planning pass), with aliased blocks, padded tokens,
+call paths (cluster split, one CTA per token, planning pass), with aliased blocks, padded tokens,
 negative positions and missing kv slots. On half the cases a few tokens get out-of-range
 request rows, block ids, block-table columns or kv slots: the device error bits and the stored
 set must then equal the oracle's. Every case passes the two-level parity."""

@@ -1,7 +1,7 @@
 """Long contexts: window ends spread up to position 1,048,575 (a block table of 131,088 columns, a
 cos/sin cache of 1,048,704 rows), so the window start, the block-table column, the cos/sin row and
 every address built from them are far past the ranges of the other workloads.
-- C128: one case per launch mode, cluster split (100 tokens), token striding (300), planning pass
+- C128: one case per launch mode, cluster split (100 tokens), one CTA per token (300), planning pass
   and window queue (2000); random requests, padded tokens, negative positions and missing kv
   slots as in the other random problems.
 - The other configurations (C4 sparse, C4 indexer FP8 and MXFP4, ratio-128 indexer): one-token

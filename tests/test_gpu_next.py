@@ -65,13 +65,13 @@ def test_c128_config_through_ex_is_the_c128_call():
 
 
 @pytest.mark.parametrize("sblk", [16, 24, 64, 128, 256, 12, 20])
-@pytest.mark.parametrize("shape", ["direct", "striding", "planned"])
+@pytest.mark.parametrize("shape", ["direct", "per_token", "planned"])
 def test_c128_config_with_other_block_sizes(sblk, shape):
     """C128 sizes with state blocks other than 8 rows: multiples of 8 take the C128 kernels (a
     window's 8-row chunks sit at row q0 % sblk of block q0 / sblk), others the generic kernel; each
-    launch mode of the C128 kernels (cluster split up to #SM tokens, token striding up to 8 per SM,
+    launch mode of the C128 kernels (cluster split up to #SM tokens, one CTA per token up to 8 per SM,
     then the planning pass), checked against the oracle."""
-    reqs, lo, hi = {"direct": (1, 128, 128), "striding": (1, 600, 600), "planned": (3, 128, 3000)}[shape]
+    reqs, lo, hi = {"direct": (1, 128, 128), "per_token": (1, 600, 600), "planned": (3, 128, 3000)}[shape]
     p = inputs.prefill_problem(f"c128b{sblk}", 5 + sblk, reqs, lo, hi, 512, 128, 0, 0, state_block=sblk,
                                decode_tail=20)
     kc, comp, err = run_gpu_ex(p)

@@ -290,7 +290,7 @@ def test_streams_graphs_and_timer():
     assert ref is not None
 
 
-@pytest.mark.parametrize("tokens", [300, 2000])  # token striding; memset + planning pass + PDL
+@pytest.mark.parametrize("tokens", [300, 2000])  # one CTA per token; planning pass + PDL
 def test_graph_capture_c128_paths(tokens):
     import torch
     from deepseek_v4_sparse_c128_gb300 import binding

@@ -1,4 +1,4 @@
-"""Programmatic dependent launch between calls. The cluster-split and token-striding kernels are
+"""Programmatic dependent launch between calls. The cluster-split and one-CTA-per-token kernels are
 launched as programmatic dependents of whatever kernel precedes them on the stream and let their
 own successor launch early; each waits for its predecessor to complete before it reads or writes
 global memory. These tests put that order under load: back-to-back calls that write the same
@@ -12,7 +12,7 @@ from gpu_util import to_device
 
 pytestmark = pytest.mark.gpu
 
-SIZES = [1, 16, 128, 300, 1216]  # cluster split (S = 8, 8, 1), token striding
+SIZES = [1, 16, 128, 300, 1216]  # cluster split (S = 8, 8, 1), one CTA per token
 
 
 @pytest.fixture(scope="module")

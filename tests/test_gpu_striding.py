@@ -1,7 +1,7 @@
-"""The C128 kernel's token-striding mode (more tokens than SMs, at most 8 per SM: CTA c scans
-tokens c, c + #SM, ... itself, with no planning pass): few active windows among many tokens (most
-CTAs find nothing), calls enqueued back to back on one stream with different active sets, and bad
-indices followed by a clean call on the same stream."""
+"""The C128 calls with more tokens than SMs and at most 8 per SM (one CTA per token, two per SM,
+with no planning pass): few active windows among many tokens (most CTAs find nothing), calls
+enqueued back to back on one stream with different active sets, and bad indices followed by a
+clean call on the same stream; and a batch beyond the per-chunk planning pass's range."""
 import numpy as np
 import pytest
 

@@ -25,7 +25,7 @@ def binding():
     return b
 
 
-@pytest.mark.parametrize("tokens", [300, 2000])  # token striding; planning pass + window queue
+@pytest.mark.parametrize("tokens", [300, 2000])  # one CTA per token; planning pass + window queue
 def test_stalled_stage_times_out_and_the_context_survives(binding, tokens):
     import torch
     p = inputs.make_problem("sweep", tokens=tokens)

@@ -68,11 +68,11 @@ def test_noalloc_refuses_batches_beyond_its_static_array(binding):
     assert np.array_equal(d["k_cache"].cpu().numpy(), p.k_cache)
 
 
-def test_noalloc_allocates_nothing_and_covers_token_striding(binding):
+def test_noalloc_allocates_nothing_and_covers_one_cta_per_token(binding):
     """After one warm-up call (the first call on a device loads the library's static array and
     looks up its address), two more calls on a stream the allocating entry point never used leave
     the device's free memory and torch's reserved memory exactly as they were. The batch has twice
-    as many tokens as the GPU has SMs, which runs the compress kernel in token-striding mode."""
+    as many tokens as the GPU has SMs, which runs one CTA per token (two per SM)."""
     import torch
     sm = torch.cuda.get_device_properties(0).multi_processor_count
     p = inputs.make_problem("sweep", tokens=2 * sm)
