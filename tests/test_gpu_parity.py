@@ -36,7 +36,7 @@ def test_workload_parity(name):
         assert 10 <= rep["stored"] <= 60
 
 
-@pytest.mark.parametrize("T", [1, 2, 3, 5, 19, 20, 38, 39, 64, 76, 77, 127, 151, 152, 153, 300, 600, 1000, 1216, 1217, 2000])
+@pytest.mark.parametrize("T", [1, 2, 3, 5, 19, 20, 38, 39, 64, 76, 77, 127, 151, 152, 153, 200, 256, 300, 600, 1000, 1216, 1217, 2000])
 def test_sweep_sizes(T):
     """All-boundary tokens: every launch mode (cluster split S = 8, 4, 2, 1 for T x S <= #SM,
     then the planned persistent path, whose windows are split into 8, 4, 2 or 1 parts merged
