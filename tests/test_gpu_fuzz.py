@@ -7,7 +7,12 @@ indexer ring, gather). compress_norm_rope_store: random batches of 1..5000 token
 call paths (cluster split, one CTA per token, planning pass), with aliased blocks, padded tokens,
 negative positions and missing kv slots. On half the cases a few tokens get out-of-range
 request rows, block ids, block-table columns or kv slots: the device error bits and the stored
-set must then equal the oracle's. Every case passes the two-level parity."""
+set must then equal the oracle's. Every case passes the two-level parity.
+
+C128_FUZZ_ROUNDS=k (environment) runs k times as many cases of both generators (new seeds
+after the default ones), for soak runs."""
+import os
+
 import numpy as np
 import pytest
 
@@ -58,7 +63,10 @@ def _case_ex(i: int):
                 tail=int(rng.integers(0, 30)), seed=int(rng.integers(1 << 30)))
 
 
-@pytest.mark.parametrize("i", range(48))
+_ROUNDS = max(1, int(os.environ.get("C128_FUZZ_ROUNDS", "1")))
+
+
+@pytest.mark.parametrize("i", range(48 * _ROUNDS))
 def test_random_configuration(i):
     c = _case_ex(i)
     p = inputs.prefill_problem("fuzz", c["seed"], c["reqs"], 1, c["maxlen"], c["head"], c["ratio"], c["overlap"],
@@ -72,7 +80,7 @@ def test_random_configuration(i):
         assert err == 0, c
 
 
-@pytest.mark.parametrize("i", range(32))
+@pytest.mark.parametrize("i", range(32 * _ROUNDS))
 def test_random_c128_batch(i):
     rng = np.random.default_rng([128, i])
     T = int(rng.choice([int(rng.integers(1, 160)), int(rng.integers(150, 1300)), int(rng.integers(1200, 5000))]))
