@@ -717,9 +717,9 @@ __global__ void __launch_bounds__(SmallGeo<HEAD>::kThreads, 1)
   // A programmatic dependent of the kernel before it on the stream (with token striding the
   // previous call's kernel or whatever precedes the call, on the planned path the planning pass,
   // which itself waits for the kernel before it): nothing global is touched before that kernel has
-  // completed. The next launch may start as soon as every CTA of this one runs.
+  // completed (the barriers, in shared memory, are set up while it runs). The next launch may
+  // start as soon as every CTA of this one runs.
   launch_dependents();
-  grid_dependency_wait();
   if (tid == 0) {
     for (int s = 0; s < G::kStages; ++s) {
       mbar_init(&S.full[s], 1);
@@ -733,6 +733,7 @@ __global__ void __launch_bounds__(SmallGeo<HEAD>::kThreads, 1)
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
+  grid_dependency_wait();
   // tiled loads need 128-byte aligned destinations (every stage offset is a multiple of 1 KiB)
   const bool use_tiled = (flags & kFlagTiled) != 0 && (smem_addr(smem_raw) & 127u) == 0u;
   if (warp == 0) {

@@ -451,9 +451,9 @@ __global__ void __launch_bounds__(kIxThreads, 1)
   // A programmatic dependent of the kernel before it on the stream (with token striding the
   // previous call's kernel or whatever precedes the call, on the planned path the planning pass,
   // which itself waits for the kernel before it): nothing global is touched before that kernel has
-  // completed. The next launch may start as soon as every CTA of this one runs.
+  // completed (the barriers, in shared memory, are set up while it runs). The next launch may
+  // start as soon as every CTA of this one runs.
   launch_dependents();
-  grid_dependency_wait();
   if (tid == 0) {
     for (int s = 0; s < kIxStages; ++s) {
       mbar_init(&S.full[s], 1);
@@ -471,6 +471,7 @@ __global__ void __launch_bounds__(kIxThreads, 1)
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
+  grid_dependency_wait();
   if (warp == 0) {
     if (p.strided)
       ix_scheduler<FMT, true>(p, S, lane);

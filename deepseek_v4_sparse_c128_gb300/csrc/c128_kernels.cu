@@ -358,10 +358,10 @@ __global__ void __launch_bounds__(kThreads, 1) compress_kernel(Params p) {
   Smem& S = *reinterpret_cast<Smem*>(smem_raw);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // Launched as a programmatic dependent of the planning pass, which itself waits for the kernel
-  // before it: nothing global is touched before that pass has completed. The next launch may
-  // start as soon as every CTA of this one runs.
+  // before it: nothing global is touched before that pass has completed (the barriers, in shared
+  // memory, are set up while it runs). The next launch may start as soon as every CTA of this one
+  // runs.
   launch_dependents();
-  grid_dependency_wait();
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&S.full[s], 1);
@@ -375,6 +375,7 @@ __global__ void __launch_bounds__(kThreads, 1) compress_kernel(Params p) {
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
+  grid_dependency_wait();
   if (warp == 0) {
     scheduler_warp<ANY>(p, S, lane);
   } else if (warp == 1) {
