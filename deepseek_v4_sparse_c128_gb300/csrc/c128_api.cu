@@ -269,7 +269,7 @@ int run(const c128_tensor_t* ttr, const c128_tensor_t* pos, const c128_tensor_t*
     C128_TRY(device_info(dev, &di));
     C128_TRY(workspace_for(dev, stream, c128::plan_list_entries(T), &p.ws));
     cfg.sm_count = di->sm_count;
-    // the C128 stall test needs the compress kernel: batches of more tokens than SMs
+    // the C128 stall test needs the one-CTA-per-token or the compress kernel: more tokens than SMs
     if (stall_test && config == nullptr && T <= di->sm_count) return C128_ERR_ARG;
     const int64_t g = static_cast<int64_t>(di->sm_count) * di->ctas_per_sm;
     cfg.grid = static_cast<int>(T < g ? T : g);

@@ -151,7 +151,8 @@ int compress_norm_rope_store(const c128_tensor_t* token_to_req_indices,
 /*
  * Test of the failure handling, for tests only. Runs compress_norm_rope_store on the same
  * arguments (C128 layout), except that CTA 0 arms the first stage of its first window and never
- * copies into it (the one-CTA-per-token kernel up to 8 tokens per SM, the compress kernel above).
+ * copies into it (the one-CTA-per-token kernel up to 8 tokens per SM, where CTA 0 has a window only
+ * if token 0 is active; the compress kernel above).
  * Every wait in the kernels is bounded (1 s), so the consumers of that stage give up, the CTA
  * stops, and the kernel ends with C128_DEV_TIMEOUT in the device error bits (read them with
  * c128_device_errors) instead of hanging; the CUDA context stays usable. Other CTAs store their
