@@ -77,18 +77,22 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(Params p) {
 // the list order does not depend on which CTA finishes first. It is launched as a programmatic
 // dependent of the kernel before it (the previous call's compress kernel still reads the list and
 // the claim counter until it completes): it waits for that kernel before any global access.
-__global__ void __launch_bounds__(kPlanThreads) plan_chunks_kernel(Params p) {
+// THREADS threads per CTA (256 or 512), kPlanTokensPerCta / THREADS tokens each.
+template <int THREADS>
+__global__ void __launch_bounds__(THREADS) plan_chunks_kernel(Params p) {
+  constexpr int kTok = kPlanTokensPerCta / THREADS;
+  static_assert(kTok * THREADS == kPlanTokensPerCta && kTok <= 32, "whole chunks, one flag bit per token");
   launch_dependents();
   grid_dependency_wait();
-  __shared__ uint32_t warp_base[kPlanThreads / 32];
+  __shared__ uint32_t warp_base[THREADS / 32];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t base = static_cast<int64_t>(blockIdx.x) * kPlanTokensPerCta;
   if (blockIdx.x == 0 && tid == 0) p.ws->next = 0u;
-  // thread tid takes tokens base + 8 tid .. + 7, so that the list comes out in token order
+  // thread tid takes tokens base + kTok tid .. + kTok - 1, so that the list comes out in token order
   uint32_t flags = 0;
 #pragma unroll
-  for (int i = 0; i < kPlanTokensPerThread; ++i) {
-    const int64_t t = base + static_cast<int64_t>(tid) * kPlanTokensPerThread + i;
+  for (int i = 0; i < kTok; ++i) {
+    const int64_t t = base + static_cast<int64_t>(tid) * kTok + i;
     if (t < p.T) {
       const int64_t s = __ldg(p.slot + t), pos = __ldg(p.pos + t), kv = __ldg(p.kvslot + t);
       const bool active = (s >= 0) & (pos >= 0) & (((pos + 1) & (p.ratio - 1)) == 0) & (kv >= 0);
@@ -106,16 +110,15 @@ __global__ void __launch_bounds__(kPlanThreads) plan_chunks_kernel(Params p) {
   __syncthreads();
   uint32_t out = incl - n, total = 0;
 #pragma unroll
-  for (int w = 0; w < kPlanThreads / 32; ++w) {
+  for (int w = 0; w < THREADS / 32; ++w) {
     const uint32_t c = warp_base[w];
     if (w < warp) out += c;
     total += c;
   }
   int32_t* list = reinterpret_cast<int32_t*>(p.ws + 1);
 #pragma unroll
-  for (int i = 0; i < kPlanTokensPerThread; ++i)
-    if ((flags >> i) & 1u)
-      list[base + out++] = static_cast<int32_t>(base + static_cast<int64_t>(tid) * kPlanTokensPerThread + i);
+  for (int i = 0; i < kTok; ++i)
+    if ((flags >> i) & 1u) list[base + out++] = static_cast<int32_t>(base + static_cast<int64_t>(tid) * kTok + i);
   if (tid == 0) list[p.T + blockIdx.x] = static_cast<int32_t>(total);
 }
 
@@ -699,22 +702,25 @@ namespace {
 // kernel before it (it launches while that kernel finishes and waits for it before any global
 // access). Not behind the head-512 small-window kernel: there every call took about 20 us longer
 // than its kernel (the 832-thread CTAs and the early pass did not overlap; measured, not
-// explained), against 1 us without the early launch.
-cudaError_t launch_plan(const Params& p, const LaunchCfg& cfg, cudaStream_t stream, Params* q, bool early) {
+// explained), against 1 us without the early launch. `wide`: 512 threads of 4 tokens per chunk
+// instead of 256 of 8 (1.0-1.8 us less per planned call, but 2.7 us more behind the head-128
+// small-window kernel, whose CTAs the early 512-thread CTAs then sit beside).
+cudaError_t launch_plan(const Params& p, const LaunchCfg& cfg, cudaStream_t stream, Params* q, bool early,
+                        bool wide) {
   const int plan_grid = static_cast<int>((p.T + kPlanTokensPerCta - 1) / kPlanTokensPerCta);
   *q = p;
   q->chunked = plan_grid <= kMaxPlanChunks;
   if (q->chunked) {
     cudaLaunchConfig_t pc = {};
     pc.gridDim = dim3(static_cast<unsigned>(plan_grid));
-    pc.blockDim = dim3(kPlanThreads);
+    pc.blockDim = dim3(wide ? 512 : 256);
     pc.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     pc.attrs = attr;
     pc.numAttrs = cfg.pdl && early ? 1 : 0;
-    return cudaLaunchKernelEx(&pc, plan_chunks_kernel, *q);
+    return wide ? cudaLaunchKernelEx(&pc, plan_chunks_kernel<512>, *q) : cudaLaunchKernelEx(&pc, plan_chunks_kernel<256>, *q);
   }
   cudaError_t e = cudaMemsetAsync(p.ws, 0, 2 * sizeof(unsigned int), stream);  // count, next
   if (e != cudaSuccess) return e;
@@ -740,7 +746,9 @@ cudaError_t launch(const Params& p, const LaunchCfg& cfg, cudaStream_t stream) {
       }
     }
     Params q;
-    if ((e = launch_plan(p, cfg, stream, &q, !(small_window_path(p) && p.head == kHead))) != cudaSuccess) return e;
+    const bool small = small_window_path(p);
+    if ((e = launch_plan(p, cfg, stream, &q, !(small && p.head == kHead), !(small && p.head != kHead))) != cudaSuccess)
+      return e;
     if (cfg.ev_begin != nullptr && (e = cudaEventRecord(cfg.ev_begin, stream)) != cudaSuccess) return e;
     if (small_window_path(q)) {
       e = launch_small(q, cfg, stream);
@@ -766,7 +774,7 @@ cudaError_t launch(const Params& p, const LaunchCfg& cfg, cudaStream_t stream) {
   if (p.T <= static_cast<int64_t>(kStridedTokensPerSm) * cfg.sm_count)
     return any_block ? launch_direct<1, true, kMidRing>(p, cfg, stream) : launch_direct<1, false, kMidRing>(p, cfg, stream);
   Params q;
-  e = launch_plan(p, cfg, stream, &q, true);
+  e = launch_plan(p, cfg, stream, &q, true, true);
   if (e != cudaSuccess) return e;
   if (cfg.ev_begin != nullptr && (e = cudaEventRecord(cfg.ev_begin, stream)) != cudaSuccess) return e;
   cudaLaunchConfig_t lc = {};
