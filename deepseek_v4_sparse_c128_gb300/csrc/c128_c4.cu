@@ -182,7 +182,7 @@ __device__ void small_scheduler(const Params& p, SmallSmem<HEAD>& S, int lane, b
   // claim size: 32 windows when there is plenty of work, else about one claim per CTA, so that a
   // small batch spreads over the SMs instead of a few CTAs taking 32 windows each
   const uint32_t per_cta = (A + gridDim.x - 1) / gridDim.x;
-  const uint32_t batch = per_cta >= static_cast<uint32_t>(kBatch) ? static_cast<uint32_t>(kBatch) : max(per_cta, 1u);
+  uint32_t batch = per_cta >= static_cast<uint32_t>(kBatch) ? static_cast<uint32_t>(kBatch) : max(per_cta, 1u);
   int64_t next_t = blockIdx.x;
   bool stall_pending = strided && p.stall_first_window && blockIdx.x == 0;
   bool failed = false;
@@ -198,6 +198,14 @@ __device__ void small_scheduler(const Params& p, SmallSmem<HEAD>& S, int lane, b
     uint32_t base = 0;
     if (!strided && lane == 0) base = atomicAdd(&p.ws->next, batch);
     base = __shfl_sync(0xffffffffu, base, 0);
+    // this claim takes windows base .. base + claim - 1; the next one is sized by what is left after
+    // it (guided: about half a share per CTA, at most kBatch), so the last claims of a call are small
+    // and the CTAs finish together. A window's stage and group do not depend on the claim sizes.
+    const uint32_t claim = batch;
+    if (!strided) {
+      const uint32_t left = A > base + claim ? A - (base + claim) : 0u;
+      batch = min(static_cast<uint32_t>(kBatch), max(1u, left / (2u * gridDim.x)));
+    }
     if (strided ? next_t >= p.T : base >= A) {
       if (lane == 0) S.qcount[qs] = -1;
       mbar_arrive(&S.qfull[qs]);
@@ -216,7 +224,7 @@ __device__ void small_scheduler(const Params& p, SmallSmem<HEAD>& S, int lane, b
         live = (sl >= 0) & (ps >= 0) & (((ps + 1) & (p.ratio - 1)) == 0) & (kv >= 0);
       }
     } else {
-      live = a < A && static_cast<uint32_t>(lane) < batch;
+      live = a < A && static_cast<uint32_t>(lane) < claim;
       if (live) t = plan_token(p, S.chunk_prefix, a);
     }
     int req = 0, nvalid = 0, ngroups = 0;
