@@ -199,12 +199,14 @@ __device__ void small_scheduler(const Params& p, SmallSmem<HEAD>& S, int lane, b
     if (!strided && lane == 0) base = atomicAdd(&p.ws->next, batch);
     base = __shfl_sync(0xffffffffu, base, 0);
     // this claim takes windows base .. base + claim - 1; the next one is sized by what is left after
-    // it (guided: about half a share per CTA, at most kBatch), so the last claims of a call are small
-    // and the CTAs finish together. A window's stage and group do not depend on the claim sizes.
+    // it (guided: a half share per CTA for head 128, a third with at least 2 windows for head 512,
+    // at most kBatch), so the last claims of a call are small and the CTAs finish together. A
+    // window's stage and group do not depend on the claim sizes.
     const uint32_t claim = batch;
     if (!strided) {
+      constexpr uint32_t kDiv = HEAD == 512 ? 3u : 2u, kMin = HEAD == 512 ? 2u : 1u;
       const uint32_t left = A > base + claim ? A - (base + claim) : 0u;
-      batch = min(static_cast<uint32_t>(kBatch), max(1u, left / (2u * gridDim.x)));
+      batch = min(static_cast<uint32_t>(kBatch), max(kMin, left / (kDiv * gridDim.x)));
     }
     if (strided ? next_t >= p.T : base >= A) {
       if (lane == 0) S.qcount[qs] = -1;
