@@ -292,3 +292,18 @@ def test_read_probe_validation(L, args, code):
 def test_read_probe_null_result_word(L):
     assert L.c128_read_probe(FAKE, 64, 512, 2, 8, None, None) == 1
     assert L.c128_read_probe(FAKE, 64, 512, 2, 8, FAKE + 2, None) == 5
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    """Without the built library the binding raises at load: there is no other path to fall back
+    to (run in a fresh interpreter, since this process has the library loaded already)."""
+    import subprocess
+    import sys
+    code = ("from deepseek_v4_sparse_c128_gb300 import binding\n"
+            "try:\n"
+            f"    binding.load({str(tmp_path / 'libc128compress.so')!r})\n"
+            "except RuntimeError as e:\n"
+            "    print('raised', 'not found' in str(e))\n")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    out = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, cwd=root, timeout=300)
+    assert out.stdout.strip() == "raised True", out.stdout + out.stderr
